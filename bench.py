@@ -1,0 +1,425 @@
+"""Benchmark of linear_logp on GB300: tokens/s of forward + backward at the
+Qwen3-8B output-layer shape, with the tensor-core roofline fraction.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl rlk|reference]
+                [--workload qwen3_8b|qwen3_30b_tp2|tiny] [--quick]
+
+A step is one pass of the whole path over one synthetic batch: the fused
+forward (tile GEMM + online statistics + fixed-tree merge; for the sharded
+workload one call per vocab shard plus rlk_lse_merge) and the backward (dz
+recompute, dH, dW; sharded: per shard plus the fixed-order dH sum). N > 1
+runs one independent batch per rank (weak scaling; no collective on the data
+path, only a barrier and a max of the elapsed times). Rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU oracle on the host cores instead (each
+step a bounded sample of the same workload, extrapolated per token).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi sampling (every 200 ms) of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        self.path = None
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="rlk_clocks_", suffix=".csv")
+            self.out = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", gpu_id], stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+
+def oracle_sample_rate(w: workloads.Workload, d: dict, n_tok: int = 16, n_vrows: int = 1024,
+                       seed: int = 0):
+    """Oracle (fp64, all host cores) fwd+bwd throughput on a bounded sample.
+
+    n_tok sampled tokens go through the oracle's forward and dH; dW is
+    evaluated for n_vrows sampled vocab rows (with g restricted to the sampled
+    tokens) and its time scaled by V / n_vrows. Returns (tokens/s, cores, sample text).
+    """
+    import oracle
+    oracle.build()
+    rows = workloads.sample_rows(w.T, n_tok, seed=seed, stream=11)
+    vrows = workloads.sample_rows(w.V, n_vrows, seed=seed, stream=12)
+    g_sub = np.zeros(w.T, np.float64)
+    g_sub[rows] = d["g"][rows]
+    t0 = time.perf_counter()
+    _, lse_rows = oracle.forward(d["h"], d["W"], d["y"], w.V_true, rows=rows)
+    t1 = time.perf_counter()
+    oracle.backward_dh(d["h"], d["W"], d["y"], d["g"].astype(np.float64), w.V_true, rows=rows)
+    t2 = time.perf_counter()
+    lse_full = np.zeros(w.T)
+    lse_full[rows] = lse_rows
+    oracle.backward_dw(d["h"], d["W"], d["y"], g_sub, lse_full, w.V_true, vrows=vrows)
+    t3 = time.perf_counter()
+    per_step = (t1 - t0) + (t2 - t1) + (t3 - t2) * (w.V / len(vrows))
+    sample = (f"{len(rows)} of {w.T} tokens: oracle forward + dH over all {w.V_true} columns; "
+              f"dW for {len(vrows)} of {w.V} vocab rows, time scaled by {w.V / len(vrows):.1f}")
+    return len(rows) / per_step, oracle.default_threads(), sample
+
+
+def run_reference(args, w: workloads.Workload, rank: int, world: int):
+    """--impl reference: the fp64 oracle on the host cores, same metric and workload."""
+    if rank != 0:
+        return
+    d = workloads.make_inputs(w)
+    n_tok = 4 if w.T >= 4096 else min(w.T, 16)
+    for i in range(args.warmup):
+        oracle_sample_rate(w, d, n_tok=n_tok, n_vrows=256, seed=100 + i)
+    rates = []
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        r, cores, sample = oracle_sample_rate(w, d, n_tok=n_tok, n_vrows=256, seed=i)
+        rates.append(r)
+    wall = time.perf_counter() - t0
+    value = float(statistics.median(rates))
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "impl": "reference",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * w.T / value, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(w, world),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "wall_s": wall}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU path
+
+METRIC = "linear_logp tokens/s fwd & fwd+bwd at Qwen3-8B shape; % of GB300 BF16 TC roofline"
+
+
+def config_dict(w: workloads.Workload, world: int):
+    return {"workload": f"{w.name} fwd+bwd T={w.T} H={w.H} V={w.V} V_true={w.V_true}"
+                        + (f" shards={len(w.shards)}" if w.shards else ""),
+            "tokens_per_rank": w.T, "H": w.H, "V": w.V, "V_true": w.V_true,
+            "global_tokens": w.T * world, "parallelism": f"replicas{world}",
+            "l2_policy": "inputs larger than L2 (W alone exceeds 129 MB); no flush"}
+
+
+class Path:
+    """Device buffers and the C-ABI calls of one step."""
+
+    def __init__(self, rlk, torch, w: workloads.Workload, d: dict, device):
+        self.rlk, self.torch, self.w = rlk, torch, w
+        bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)  # noqa: E731
+        self.h = bf(d["h"])
+        self.W = bf(d["W"]) if "W" in d else None
+        self.y = torch.from_numpy(d["y"]).to(device)
+        self.g = torch.from_numpy(d["g"]).to(device)
+        T, H, V = w.T, w.H, w.V
+        f32 = torch.float32
+        self.logp = torch.empty(T, dtype=f32, device=device)
+        self.lse = torch.empty(T, dtype=f32, device=device)
+        self.dW = torch.empty((V, H), dtype=f32, device=device)
+        shards = w.shards or ((0, V),)
+        self.shards = shards
+        self.fws = torch.empty(max(rlk.fwd_workspace_bytes(T, H, n) for _, n in shards),
+                               dtype=torch.uint8, device=device)
+        self.bws = torch.empty(max(rlk.bwd_workspace_bytes(T, H, n) for _, n in shards),
+                               dtype=torch.uint8, device=device)
+        if w.shards:
+            self.parts = torch.empty((len(shards), T, 3), dtype=f32, device=device)
+            self.dH_parts = torch.empty((len(shards), T, H), dtype=f32, device=device)
+            self.dH = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        else:
+            self.dH = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+
+    def launches_per_step(self):
+        n = len(self.shards)
+        return (2 * n + 1 + 3 * n + 1) if self.w.shards else 5
+
+    def forward(self):
+        rlk, w = self.rlk, self.w
+        if not w.shards:
+            rlk.linear_logp_fwd(self.h, self.W, self.y, w.V_true, out=(self.logp, self.lse),
+                                workspace=self.fws)
+        else:
+            for i, (a, n) in enumerate(self.shards):
+                rlk.linear_logp_fwd(self.h, self.W[a:a + n], self.y, w.V_true, vocab_start=a,
+                                    partial=True, out=(self.parts[i],), workspace=self.fws)
+            rlk.lse_merge(self.parts, out=(self.logp, self.lse))
+
+    def backward(self):
+        rlk, w = self.rlk, self.w
+        if not w.shards:
+            rlk.linear_logp_bwd(self.h, self.W, self.y, self.lse, self.g, w.V_true,
+                                out=(self.dH, self.dW), workspace=self.bws)
+        else:
+            for i, (a, n) in enumerate(self.shards):
+                rlk.linear_logp_bwd(self.h, self.W[a:a + n], self.y, self.lse, self.g, w.V_true,
+                                    vocab_start=a, dH_fp32_partial=True,
+                                    out=(self.dH_parts[i], self.dW[a:a + n]), workspace=self.bws)
+            rlk.shard_sum_bf16(self.dH_parts, out=self.dH)
+
+
+def gpu_uuid(torch, device):
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        return str(device.index or 0)
+
+
+def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int):
+    import torch
+
+    import deterministic_token_logprob_gb300 as rlk
+    from deterministic_token_logprob_gb300 import build as libbuild
+    if rank == 0 or world == 1:
+        libbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    peaks, peaks_src = load_peaks()
+
+    # model weight shared by all ranks (seed 0); each rank its own batch
+    W_bits = workloads.make_W(w.V, w.H, seed=0)
+    wr = workloads.Workload(w.name, T=w.T, H=w.H, V=w.V, V_true=w.V_true, seed=rank,
+                            g_kind=w.g_kind, shards=w.shards)
+    d = workloads.make_inputs(wr, with_W=False)
+    d["W"] = W_bits
+    path = Path(rlk, torch, wr, d, device)
+    stream = torch.cuda.current_stream(device)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        path.forward()
+        path.backward()
+    torch.cuda.synchronize(device)
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    sampler = ClockSampler(gpu_uuid(torch, device)) if rank == 0 else None
+    barrier()
+    torch.cuda.synchronize(device)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        path.forward()
+        ev[i][1].record(stream)
+        path.backward()
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(device)
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    total_ms = t_start.elapsed_time(t_end)
+    fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    tokens_per_s = w.T * world * K / (total_ms / 1e3)
+
+    flops_fwd = 2.0 * w.T * w.H * w.V_true
+    fwd_avg = statistics.mean(fwd_ms)
+    achieved = flops_fwd / (fwd_avg / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    step_flops = 3.0 * flops_fwd
+    roofline_ms = step_flops / (peak * 1e12) * 1e3
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(w, world),
+        "gpu_launches": K * path.launches_per_step(),
+        "roofline": {"bound": "tensor", "kernel": "forward tile GEMM + online statistics",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_source": f"{peaks_src} bf16 burst",
+                     "algorithmic_flops_per_launch": flops_fwd, "avg_launch_ms": fwd_avg},
+        "step_roofline": {"flops_counted": step_flops, "roofline_ms": roofline_ms,
+                          "frac_of_burst": roofline_ms / ms_per_step,
+                          "frac_of_sustained": (step_flops / (peak_sus * 1e12) * 1e3) / ms_per_step,
+                          "fwd_ms": fwd_avg, "bwd_ms": statistics.mean(bwd_ms)},
+        "clocks": clocks,
+    }
+
+    if rank == 0 and world == 1 and not args.quick:
+        line["fwd_only"] = fwd_only(rlk, torch, W_bits, path, device, args, peak)
+        line["e2e"] = e2e(rlk, torch, path, wr, d, device, args)
+        rate, cores, sample = oracle_sample_rate(wr, d)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def fwd_only(rlk, torch, W_bits, path, device, args, peak):
+    """Forward-only tokens/s on the Qwen3-8B forward workload (T=4096), same W."""
+    w = workloads.QWEN3_8B_FWD
+    h = torch.from_numpy(workloads.make_h(w.T, w.H, 0).view(np.int16)).view(torch.bfloat16).to(device)
+    y = torch.from_numpy(workloads.make_y(w.T, w.V_true, 0)).to(device)
+    logp = torch.empty(w.T, dtype=torch.float32, device=device)
+    lse = torch.empty(w.T, dtype=torch.float32, device=device)
+    ws = torch.empty(rlk.fwd_workspace_bytes(w.T, w.H, w.V), dtype=torch.uint8, device=device)
+    W = path.W
+    for _ in range(max(3, args.warmup)):
+        rlk.linear_logp_fwd(h, W, y, w.V_true, out=(logp, lse), workspace=ws)
+    K = max(args.steps, 10)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    a.record()
+    for _ in range(K):
+        rlk.linear_logp_fwd(h, W, y, w.V_true, out=(logp, lse), workspace=ws)
+    b.record()
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / K
+    tf = 2.0 * w.T * w.H * w.V_true / (ms / 1e3) / 1e12
+    return {"workload": f"{w.name} T={w.T} H={w.H} V={w.V} V_true={w.V_true}",
+            "tokens_per_s": w.T / (ms / 1e3), "ms_per_call": ms, "tflops": tf,
+            "frac_of_burst": tf / peak, "steps": K}
+
+
+def e2e(rlk, torch, path, w, d, device, args):
+    """Same step through the public API from pinned host buffers: H2D of the
+    step's inputs (h, y, g), the C-ABI calls, D2H of the result (logp). The
+    weight W is model state and stays resident, as in a training step."""
+    h_host = torch.from_numpy(d["h"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_host = torch.from_numpy(d["y"]).pin_memory()
+    g_host = torch.from_numpy(d["g"]).pin_memory()
+    logp_host = torch.empty(w.T, dtype=torch.float32).pin_memory()
+    h2d = h_host.numel() * 2 + y_host.numel() * 8 + g_host.numel() * 4
+    d2h = logp_host.numel() * 4
+
+    def step():
+        path.h.copy_(h_host, non_blocking=True)
+        path.y.copy_(y_host, non_blocking=True)
+        path.g.copy_(g_host, non_blocking=True)
+        path.forward()
+        path.backward()
+        logp_host.copy_(path.logp, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(device)
+    K = args.steps
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(K):
+        step()
+    b.record()
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / K
+    return {"value": w.T / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["rlk", "reference"], default="rlk")
+    ap.add_argument("--workload", choices=["qwen3_8b", "qwen3_30b_tp2", "tiny"], default="qwen3_8b")
+    ap.add_argument("--quick", action="store_true", help="skip the forward-only, e2e and CPU legs")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = workloads.CONFIGS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_gpu(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

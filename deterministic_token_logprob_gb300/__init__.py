@@ -1,0 +1,13 @@
+"""deterministic_token_logprob_gb300 -- deterministic, batch-invariant `linear_logp` on GB300.
+
+The operator returns logp[t] = h_t . W_{y_t} - logsumexp_{v < V_true}(h_t . W_v)
+(fp32) without materialising the [T, V] logits, plus dH / dW of
+sum_t g_t logp_t. It is a C ABI shared library (include/rlk.h, built into
+``_build/librlk.so`` from ``csrc/``) with hand-written sm_103a kernels
+(tcgen05 / TMEM / TMA); this package is its thin ctypes binding.
+"""
+from ._binding import (  # noqa: F401
+    LEAF_WIDTH, MAX_SHARDS, RLK_ERR_CUDA, RLK_ERR_INVALID_ARG, RLK_ERR_UNSUPPORTED,
+    RLK_ERR_WORKSPACE, RLK_FLAG_BAD_TARGET, RLK_FLAG_TIMEOUT, RLK_OK, RlkError,
+    bwd_workspace_bytes, fwd_workspace_bytes, lib, library_path, linear_logp_bwd, linear_logp_fwd,
+    lse_merge, shard_bounds, shard_sum_bf16, version)

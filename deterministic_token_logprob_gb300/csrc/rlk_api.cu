@@ -1,0 +1,490 @@
+// rlk_api.cu -- the C ABI of include/rlk.h: argument validation, workspace
+// carve-up, tensor-map encoding and kernel launches, plus the small kernels
+// of the fixed merge tree (leaf tree, shard merge, shard sum).
+//
+// Nothing here allocates device or host memory, synchronises the host, or
+// keeps state between calls beyond a cached driver entry point.
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "rlk.h"
+#include "rlk_internal.h"
+#include "rlk_ptx.cuh"
+
+namespace rlk {
+namespace {
+
+// ---------------------------------------------------------------------------
+// The merge operator of the statistics triples and the final step.
+// ("Why the Fused Path Wins", third reason: shards combine only the statistics
+// needed for the global selected logprob; fixed merge order, item 3 of "The
+// Numerical Execution Contract".)
+// ---------------------------------------------------------------------------
+struct Triple {
+  float m, s, zt;
+};
+
+__device__ __forceinline__ Triple identity_triple() { return Triple{neg_inf(), 0.f, neg_inf()}; }
+
+__device__ __forceinline__ float merge_target(float a, float b) {
+  // exactly one shard owns a valid target, the others hold -inf; NaN marks an invalid target
+  return (isnan(a) || isnan(b)) ? __int_as_float(0x7fc00000) : fmaxf(a, b);
+}
+
+// a (+) b, operand a's term first. An operand with s == 0 is the identity (an
+// empty shard or a padding slot) and leaves the other unchanged, bit for bit.
+__device__ __noinline__ Triple merge_pair(Triple a, Triple b) {
+  Triple r;
+  if (a.s == 0.f) {
+    r.m = b.m;
+    r.s = b.s;
+  } else if (b.s == 0.f) {
+    r.m = a.m;
+    r.s = a.s;
+  } else if (a.m >= b.m) {
+    r.m = a.m;
+    r.s = __fadd_rn(a.s, __fmul_rn(b.s, exp_shifted(b.m, neg_scaled(a.m))));
+  } else {
+    r.m = b.m;
+    r.s = __fadd_rn(__fmul_rn(a.s, exp_shifted(a.m, neg_scaled(b.m))), b.s);
+  }
+  r.zt = merge_target(a.zt, b.zt);
+  return r;
+}
+
+// lse = m + log(s); logp = zt - lse.
+__device__ __noinline__ void finalize(Triple x, float* logp, float* lse) {
+  const float l = __fadd_rn(x.m, logf(x.s));
+  *lse = l;
+  *logp = __fsub_rn(x.zt, l);
+}
+
+constexpr int kMaxTreeDepth = 16;  // log2(max slots = 8 * 2048) + 1
+
+struct TreeArgs {
+  const float* ws_m;
+  const float* ws_s;
+  const float* ws_zt;  // [n_leaves_local][T]
+  int32_t T;
+  int32_t n_leaves_local, leaf0, n_leaves_global;
+  int32_t L_ss, P;                // leaves per super-shard, slots per super-shard
+  int32_t slot_begin, slot_count; // this shard's aligned slot range (slot_count a power of two)
+  const int64_t* y;
+  int32_t V_true;
+  rlk_lse_partial* partial;
+  float* logp;
+  float* lse;
+  int32_t* err_flag;
+};
+
+// One thread per token: balanced pairwise merge of the shard's slots (a
+// binary-counter walk: after slot q, merge once per trailing one bit of q).
+__global__ void leaf_tree_kernel(const TreeArgs a) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= a.T) return;
+  Triple stack[kMaxTreeDepth];
+  int sp = 0;
+  for (int q = 0; q < a.slot_count; ++q) {
+    const int slot = a.slot_begin + q;
+    const int ss = slot / a.P, jj = slot - ss * a.P;
+    const int leaf = ss * a.L_ss + jj;
+    const int ll = leaf - a.leaf0;
+    Triple node = identity_triple();
+    if (jj < a.L_ss && leaf < a.n_leaves_global && ll >= 0 && ll < a.n_leaves_local) {
+      const size_t o = static_cast<size_t>(ll) * a.T + t;
+      node = Triple{a.ws_m[o], a.ws_s[o], a.ws_zt[o]};
+    }
+    for (int idx = q; idx & 1; idx >>= 1) node = merge_pair(stack[--sp], node);
+    stack[sp++] = node;
+  }
+  Triple r = stack[0];
+  const int64_t y = a.y[t];
+  if (y < 0 || y >= a.V_true) {
+    r.zt = __int_as_float(0x7fc00000);
+    if (a.err_flag) atomicOr(a.err_flag, RLK_FLAG_BAD_TARGET);
+  }
+  if (a.partial) {
+    a.partial[t] = rlk_lse_partial{r.m, r.s, r.zt};
+  } else {
+    float lp, l;
+    finalize(r, &lp, &l);
+    if (a.logp) a.logp[t] = lp;
+    if (a.lse) a.lse[t] = l;
+  }
+}
+
+// Top levels of the same tree over S shard triples, then the final step.
+__global__ void lse_merge_kernel(const rlk_lse_partial* p, int S, int T, float* logp, float* lse) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  Triple stack[4];
+  int sp = 0;
+  for (int q = 0; q < S; ++q) {
+    const rlk_lse_partial x = p[static_cast<size_t>(q) * T + t];
+    Triple node{x.m, x.s, x.zt};
+    for (int idx = q; idx & 1; idx >>= 1) node = merge_pair(stack[--sp], node);
+    stack[sp++] = node;
+  }
+  float lp, l;
+  finalize(stack[0], &lp, &l);
+  logp[t] = lp;
+  lse[t] = l;
+}
+
+// out = bf16(((p0 + p1) + p2) + ...), four elements per thread. The vector path
+// needs every shard's row start 16-byte aligned, i.e. n % 4 == 0.
+__global__ void shard_sum_kernel(const float* p, int S, int64_t n, uint16_t* out) {
+  const int64_t i4 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
+  if (i4 >= n) return;
+  if (i4 + 4 <= n && (n & 3) == 0) {
+    float4 acc = *reinterpret_cast<const float4*>(p + i4);
+    for (int s = 1; s < S; ++s) {
+      const float4 x = *reinterpret_cast<const float4*>(p + static_cast<size_t>(s) * n + i4);
+      acc.x = __fadd_rn(acc.x, x.x);
+      acc.y = __fadd_rn(acc.y, x.y);
+      acc.z = __fadd_rn(acc.z, x.z);
+      acc.w = __fadd_rn(acc.w, x.w);
+    }
+    uint2 w;
+    w.x = pack_bf16x2(acc.x, acc.y);
+    w.y = pack_bf16x2(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(out + i4) = w;
+  } else {
+    for (int64_t i = i4; i < n; ++i) {
+      float acc = p[i];
+      for (int s = 1; s < S; ++s) acc = __fadd_rn(acc, p[static_cast<size_t>(s) * n + i]);
+      out[i] = static_cast<uint16_t>(pack_bf16x2(acc, 0.f) & 0xFFFFu);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host helpers
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// 2-D bf16 tensor [outer][inner] (inner contiguous), 128-byte swizzled boxes of
+// box_inner x box_outer elements; out-of-range elements read as zero.
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_elems,
+               uint32_t box_inner, uint32_t box_outer) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_elems * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool sm_count(int* n) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  return cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && *n > 0;
+}
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+inline int64_t next_pow2(int64_t x) {
+  int64_t p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+// Geometry of the fixed merge tree for a given V_true, and the part of it a
+// shard [vocab_start, vocab_start + V_local) owns.
+struct ShardGeom {
+  int64_t n_leaves, L_ss, P, ss_width;  // tree
+  int64_t ss0, n_ss;                    // shard's super-shards
+  int64_t leaf0, n_leaves_local;        // shard's leaves (global index of the first)
+  int64_t slot_begin, slot_count;
+  bool reaches_end;
+};
+
+rlk_status shard_geometry(int64_t V_local, int64_t vocab_start, int64_t V_true, ShardGeom* g) {
+  g->n_leaves = ceil_div(V_true, LEAF);
+  g->L_ss = ceil_div(g->n_leaves, MAX_SHARDS);
+  g->P = next_pow2(g->L_ss);
+  g->ss_width = g->L_ss * LEAF;
+  if (vocab_start % g->ss_width != 0) return RLK_ERR_UNSUPPORTED;
+  g->ss0 = vocab_start / g->ss_width;
+  if (g->ss0 >= MAX_SHARDS) return RLK_ERR_UNSUPPORTED;
+  g->reaches_end = vocab_start + V_local >= V_true;
+  if (!g->reaches_end && V_local % g->ss_width != 0) return RLK_ERR_UNSUPPORTED;
+  int64_t n = ceil_div(V_local, g->ss_width);
+  if (n > MAX_SHARDS - g->ss0) n = MAX_SHARDS - g->ss0;
+  if (g->reaches_end) n = next_pow2(n);
+  if (!is_pow2(n) || g->ss0 % n != 0 || g->ss0 + n > MAX_SHARDS) return RLK_ERR_UNSUPPORTED;
+  g->n_ss = n;
+  g->leaf0 = g->ss0 * g->L_ss;
+  const int64_t leaf_end = std::min((g->ss0 + n) * g->L_ss, g->n_leaves);
+  g->n_leaves_local = std::max<int64_t>(0, leaf_end - g->leaf0);
+  g->slot_begin = g->ss0 * g->P;
+  g->slot_count = n * g->P;
+  return RLK_OK;
+}
+
+rlk_status common_checks(const void* h, const void* W, const int64_t* y, int64_t T, int64_t H,
+                         int64_t V_local, int64_t vocab_start, int64_t V_true) {
+  // per-token inputs may be NULL for an empty batch (an empty tensor has no storage)
+  if (!W || (T > 0 && (!h || !y))) return RLK_ERR_INVALID_ARG;
+  if (T < 0 || H <= 0 || V_local <= 0 || vocab_start < 0 || V_true <= 0) return RLK_ERR_INVALID_ARG;
+  if (H % 8 != 0 || !aligned16(h) || !aligned16(W)) return RLK_ERR_INVALID_ARG;
+  if (V_true > RLK_MAX_VOCAB || V_local > RLK_MAX_VOCAB || vocab_start > RLK_MAX_VOCAB ||
+      H > RLK_MAX_HIDDEN || T > INT32_MAX - BM)
+    return RLK_ERR_UNSUPPORTED;
+  return RLK_OK;
+}
+
+size_t fwd_ws_array_bytes(int64_t T, int64_t V_local) {
+  return static_cast<size_t>(round_up(ceil_div(V_local, LEAF) * T * 4, 256));
+}
+
+}  // namespace
+}  // namespace rlk
+
+using namespace rlk;
+
+extern "C" {
+
+const char* rlk_version(void) { return "rlk 0.1.0 sm_103a"; }
+
+const char* rlk_status_string(rlk_status s) {
+  switch (s) {
+    case RLK_OK: return "ok";
+    case RLK_ERR_INVALID_ARG: return "invalid argument";
+    case RLK_ERR_UNSUPPORTED: return "unsupported shape or shard split";
+    case RLK_ERR_WORKSPACE: return "workspace missing or too small";
+    case RLK_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+size_t rlk_linear_logp_fwd_workspace(int64_t T, int64_t H, int64_t V_local) {
+  (void)H;
+  if (T <= 0 || V_local <= 0) return 0;
+  return 3 * fwd_ws_array_bytes(T, V_local);
+}
+
+rlk_status rlk_linear_logp_fwd(const void* h, const void* W, const int64_t* y, int64_t T,
+                               int64_t H, int64_t V_local, int64_t vocab_start, int64_t V_true,
+                               float* logp, float* lse, rlk_lse_partial* partial,
+                               int32_t* err_flag, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  rlk_status st = common_checks(h, W, y, T, H, V_local, vocab_start, V_true);
+  if (st != RLK_OK) return st;
+  if (!partial && !logp && !lse) return RLK_ERR_INVALID_ARG;
+  ShardGeom g;
+  st = shard_geometry(V_local, vocab_start, V_true, &g);
+  if (st != RLK_OK) return st;
+  if (!partial && (vocab_start != 0 || !g.reaches_end)) return RLK_ERR_INVALID_ARG;
+  if (T == 0) return RLK_OK;
+  const size_t arr = fwd_ws_array_bytes(T, V_local);
+  if (g.n_leaves_local > 0) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return RLK_ERR_WORKSPACE;
+    if (workspace_bytes < 3 * arr) return RLK_ERR_WORKSPACE;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* ws_m = static_cast<float*>(workspace);
+  float* ws_s = reinterpret_cast<float*>(static_cast<char*>(workspace) + arr);
+  float* ws_zt = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * arr);
+
+  if (g.n_leaves_local > 0) {
+    int n_sm = 0;
+    if (!sm_count(&n_sm)) return RLK_ERR_CUDA;
+    CUtensorMap tmA, tmB;
+    if (!encode_2d(&tmA, h, H, T, H, 64, BM)) return RLK_ERR_CUDA;
+    if (!encode_2d(&tmB, W, H, V_local, H, 64, BN)) return RLK_ERR_CUDA;
+    GemmArgs a;
+    a.T = static_cast<int32_t>(T);
+    a.H = static_cast<int32_t>(H);
+    a.V_local = static_cast<int32_t>(V_local);
+    a.vocab_start = static_cast<int32_t>(vocab_start);
+    a.V_true = static_cast<int32_t>(V_true);
+    a.n_tt = static_cast<int32_t>(ceil_div(T, BM));
+    a.leaf0 = static_cast<int32_t>(g.leaf0);
+    a.n_leaves = static_cast<int32_t>(g.n_leaves_local);
+    a.n_items = a.n_tt * a.n_leaves;
+    a.n_kb = static_cast<int32_t>(ceil_div(H, BK));
+    a.y = y;
+    a.ws_m = ws_m;
+    a.ws_s = ws_s;
+    a.ws_zt = ws_zt;
+    a.err_flag = err_flag;
+    const int grid = static_cast<int>(std::min<int64_t>(a.n_items, n_sm));
+    if (launch_gemm_fwd(tmA, tmB, a, grid, s) != cudaSuccess) return RLK_ERR_CUDA;
+  }
+
+  TreeArgs ta;
+  ta.ws_m = ws_m;
+  ta.ws_s = ws_s;
+  ta.ws_zt = ws_zt;
+  ta.T = static_cast<int32_t>(T);
+  ta.n_leaves_local = static_cast<int32_t>(g.n_leaves_local);
+  ta.leaf0 = static_cast<int32_t>(g.leaf0);
+  ta.n_leaves_global = static_cast<int32_t>(g.n_leaves);
+  ta.L_ss = static_cast<int32_t>(g.L_ss);
+  ta.P = static_cast<int32_t>(g.P);
+  ta.slot_begin = static_cast<int32_t>(g.slot_begin);
+  ta.slot_count = static_cast<int32_t>(g.slot_count);
+  ta.y = y;
+  ta.V_true = static_cast<int32_t>(V_true);
+  ta.partial = partial;
+  ta.logp = logp;
+  ta.lse = lse;
+  ta.err_flag = err_flag;
+  const int threads = 128;
+  leaf_tree_kernel<<<static_cast<unsigned>(ceil_div(T, threads)), threads, 0, s>>>(ta);
+  return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
+}
+
+rlk_status rlk_lse_merge(const rlk_lse_partial* partials, int32_t S, int64_t T, float* logp,
+                         float* lse, void* stream) {
+  if (T < 0 || (T > 0 && (!partials || !logp || !lse))) return RLK_ERR_INVALID_ARG;
+  if (S != 1 && S != 2 && S != 4 && S != 8) return RLK_ERR_UNSUPPORTED;
+  if (T > INT32_MAX) return RLK_ERR_UNSUPPORTED;
+  if (T == 0) return RLK_OK;
+  const int threads = 128;
+  lse_merge_kernel<<<static_cast<unsigned>(ceil_div(T, threads)), threads, 0,
+                     static_cast<cudaStream_t>(stream)>>>(partials, S, static_cast<int>(T), logp, lse);
+  return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
+}
+
+size_t rlk_linear_logp_bwd_workspace(int64_t T, int64_t H, int64_t V_local) {
+  (void)H;
+  if (T <= 0 || V_local <= 0) return 0;
+  return static_cast<size_t>(T) * static_cast<size_t>(round_up(V_local, BN)) * 2;
+}
+
+rlk_status rlk_linear_logp_bwd(const void* h, const void* W, const int64_t* y, const float* lse,
+                               const float* g, int64_t T, int64_t H, int64_t V_local,
+                               int64_t vocab_start, int64_t V_true, void* dH,
+                               int32_t dH_fp32_partial, float* dW, int32_t* err_flag,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  rlk_status st = common_checks(h, W, y, T, H, V_local, vocab_start, V_true);
+  if (st != RLK_OK) return st;
+  if (T > 0 && (!lse || !g)) return RLK_ERR_INVALID_ARG;
+  if ((dH && !aligned16(dH)) || (dW && !aligned16(dW))) return RLK_ERR_INVALID_ARG;
+  if (T == 0) return RLK_OK;
+  const int64_t Vd = round_up(V_local, BN);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return RLK_ERR_WORKSPACE;
+  if (workspace_bytes < rlk_linear_logp_bwd_workspace(T, H, V_local)) return RLK_ERR_WORKSPACE;
+  if (Vd > INT32_MAX / 2) return RLK_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int n_sm = 0;
+  if (!sm_count(&n_sm)) return RLK_ERR_CUDA;
+  uint16_t* dz = static_cast<uint16_t*>(workspace);
+  const int32_t n_tt = static_cast<int32_t>(ceil_div(T, BM));
+
+  // 1. recompute z tiles -> dz (bf16) workspace
+  {
+    CUtensorMap tmA, tmB;
+    if (!encode_2d(&tmA, h, H, T, H, 64, BM)) return RLK_ERR_CUDA;
+    if (!encode_2d(&tmB, W, H, V_local, H, 64, BN)) return RLK_ERR_CUDA;
+    GemmArgs a;
+    a.T = static_cast<int32_t>(T);
+    a.H = static_cast<int32_t>(H);
+    a.V_local = static_cast<int32_t>(V_local);
+    a.vocab_start = static_cast<int32_t>(vocab_start);
+    a.V_true = static_cast<int32_t>(V_true);
+    a.n_tt = n_tt;
+    a.n_items = static_cast<int32_t>(Vd / BN) * n_tt;
+    a.n_kb = static_cast<int32_t>(ceil_div(H, BK));
+    a.y = y;
+    a.lse = lse;
+    a.g = g;
+    a.dz = dz;
+    a.dz_ld = Vd;
+    a.err_flag = err_flag;
+    const int grid = static_cast<int>(std::min<int64_t>(a.n_items, n_sm));
+    if (launch_gemm_dz(tmA, tmB, a, grid, s) != cudaSuccess) return RLK_ERR_CUDA;
+  }
+
+  // 2. dH = dz W over this shard's valid columns
+  if (dH) {
+    const int64_t V_valid = std::max<int64_t>(0, std::min<int64_t>(V_true - vocab_start, V_local));
+    const size_t elem = dH_fp32_partial ? 4 : 2;
+    if (V_valid == 0) {
+      if (cudaMemsetAsync(dH, 0, static_cast<size_t>(T) * H * elem, s) != cudaSuccess) return RLK_ERR_CUDA;
+    } else {
+      CUtensorMap tmA, tmB;
+      if (!encode_2d(&tmA, dz, Vd, T, Vd, 64, BM)) return RLK_ERR_CUDA;
+      if (!encode_2d(&tmB, W, H, V_local, H, 64, 64)) return RLK_ERR_CUDA;
+      GemmArgs a;
+      a.T = static_cast<int32_t>(T);
+      a.H = static_cast<int32_t>(H);
+      a.n_mt = n_tt;
+      a.n_nt = static_cast<int32_t>(ceil_div(H, BN));
+      a.n_items = a.n_mt * a.n_nt;
+      a.n_kb = static_cast<int32_t>(ceil_div(V_valid, BK));
+      a.out = dH;
+      a.out_ld = H;
+      a.out_rows = static_cast<int32_t>(T);
+      a.out_cols = static_cast<int32_t>(H);
+      a.out_f32 = dH_fp32_partial ? 1 : 0;
+      a.err_flag = err_flag;
+      const int grid = static_cast<int>(std::min<int64_t>(a.n_items, n_sm));
+      if (launch_gemm_dh(tmA, tmB, a, grid, s) != cudaSuccess) return RLK_ERR_CUDA;
+    }
+  }
+
+  // 3. dW = dz^T h (rows at or above V_true come out exactly zero: their dz is zero)
+  if (dW) {
+    CUtensorMap tmA, tmB;
+    if (!encode_2d(&tmA, dz, Vd, T, Vd, 64, 64)) return RLK_ERR_CUDA;
+    if (!encode_2d(&tmB, h, H, T, H, 64, 64)) return RLK_ERR_CUDA;
+    GemmArgs a;
+    a.T = static_cast<int32_t>(T);
+    a.H = static_cast<int32_t>(H);
+    a.n_mt = static_cast<int32_t>(ceil_div(V_local, BM));
+    a.n_nt = static_cast<int32_t>(ceil_div(H, BN));
+    a.n_items = a.n_mt * a.n_nt;
+    a.n_kb = static_cast<int32_t>(ceil_div(T, BK));
+    a.out = dW;
+    a.out_ld = H;
+    a.out_rows = static_cast<int32_t>(V_local);
+    a.out_cols = static_cast<int32_t>(H);
+    a.out_f32 = 1;
+    a.err_flag = err_flag;
+    const int grid = static_cast<int>(std::min<int64_t>(a.n_items, n_sm));
+    if (launch_gemm_dw(tmA, tmB, a, grid, s) != cudaSuccess) return RLK_ERR_CUDA;
+  }
+  return RLK_OK;
+}
+
+rlk_status rlk_shard_sum_bf16(const float* partials, int32_t S, int64_t n, void* out, void* stream) {
+  if (!partials || !out || S < 1 || n < 0) return RLK_ERR_INVALID_ARG;
+  if (!aligned16(partials) || !aligned16(out)) return RLK_ERR_INVALID_ARG;
+  if (n == 0) return RLK_OK;
+  const int threads = 256;
+  const int64_t blocks = ceil_div(ceil_div(n, 4), threads);
+  if (blocks > INT32_MAX) return RLK_ERR_UNSUPPORTED;
+  shard_sum_kernel<<<static_cast<unsigned>(blocks), threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      partials, S, n, static_cast<uint16_t*>(out));
+  return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,11 @@
+// rlk_gemm_dh.cu -- instantiation of the tile engine for MODE_DH (see rlk_gemm.cuh).
+#include "rlk_gemm.cuh"
+
+namespace rlk {
+
+cudaError_t launch_gemm_dh(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                           int grid, cudaStream_t stream) {
+  return launch_gemm<MODE_DH>(tmA, tmB, a, grid, stream);
+}
+
+}  // namespace rlk

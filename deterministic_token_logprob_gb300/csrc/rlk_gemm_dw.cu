@@ -1,0 +1,11 @@
+// rlk_gemm_dw.cu -- instantiation of the tile engine for MODE_DW (see rlk_gemm.cuh).
+#include "rlk_gemm.cuh"
+
+namespace rlk {
+
+cudaError_t launch_gemm_dw(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                           int grid, cudaStream_t stream) {
+  return launch_gemm<MODE_DW>(tmA, tmB, a, grid, stream);
+}
+
+}  // namespace rlk

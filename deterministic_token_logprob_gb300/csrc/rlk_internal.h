@@ -1,0 +1,72 @@
+// rlk_internal.h -- host/device shared definitions of the rlk library
+// (not part of the public ABI; see include/rlk.h for that).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace rlk {
+
+// Tile constants: part of the numerical contract (they fix the K steps and the
+// vocab walk), identical for every shape.
+constexpr int BM = 128;      // tokens per tile (tcgen05 M)
+constexpr int BN = 256;      // vocab columns / output columns per tile (tcgen05 N)
+constexpr int BK = 64;       // K per pipeline stage: one 128-byte swizzle atom of bf16
+constexpr int UMMA_K = 16;   // K of one tcgen05.mma kind::f16
+constexpr int LEAF = 1024;   // vocab columns per leaf of the merge tree
+constexpr int TILES_PER_LEAF = LEAF / BN;
+constexpr int MAX_SHARDS = 8;
+
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KiB
+constexpr int B_STAGE_BYTES = BN * BK * 2;  // 32 KiB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int MN_ATOM_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) TMA box, 8 KiB
+constexpr int NUM_THREADS = 192;            // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int TMEM_COLS = 512;              // two fp32 128x256 accumulators
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /* alignment slack */ + 256 /* barriers */;
+
+enum GemmMode : int {
+  MODE_FWD = 0,  // z = h W^T per (token tile, leaf): online max / sum-exp / target
+  MODE_DZ = 1,   // z = h W^T per tile: dz = g (onehot - p) -> bf16 workspace
+  MODE_DH = 2,   // dH = dz W      (A K-major, B MN-major)
+  MODE_DW = 3,   // dW = dz^T h    (A MN-major, B MN-major)
+};
+
+struct GemmArgs {
+  int32_t T = 0, H = 0;
+  int32_t n_items = 0;
+  int32_t n_kb = 0;  // k-blocks of BK per tile
+  int32_t* err_flag = nullptr;
+  // forward / dz
+  int32_t V_local = 0, vocab_start = 0, V_true = 0;
+  int32_t n_tt = 0;                // token tiles
+  int32_t leaf0 = 0, n_leaves = 0; // fwd: global index of the shard's first leaf, leaf count
+  const int64_t* y = nullptr;
+  float* ws_m = nullptr;           // fwd: [n_leaves][T]
+  float* ws_s = nullptr;
+  float* ws_zt = nullptr;
+  const float* lse = nullptr;      // dz
+  const float* g = nullptr;
+  uint16_t* dz = nullptr;          // dz: bf16 bits [T][dz_ld]
+  int64_t dz_ld = 0;
+  // dH / dW stores
+  void* out = nullptr;
+  int64_t out_ld = 0;
+  int32_t out_rows = 0, out_cols = 0;
+  int32_t out_f32 = 0;
+  int32_t n_mt = 0, n_nt = 0;
+};
+
+// Launchers (one translation unit each), enqueue on `stream`, return the launch status.
+cudaError_t launch_gemm_fwd(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                            int grid, cudaStream_t stream);
+cudaError_t launch_gemm_dz(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                           int grid, cudaStream_t stream);
+cudaError_t launch_gemm_dh(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                           int grid, cudaStream_t stream);
+cudaError_t launch_gemm_dw(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                           int grid, cudaStream_t stream);
+
+}  // namespace rlk

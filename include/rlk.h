@@ -1,0 +1,204 @@
+/*
+ * rlk.h -- C ABI of the deterministic, batch-invariant selected-token
+ * log-probability operator `linear_logp` for NVIDIA GB300 (sm_103a).
+ *
+ * Operation ("Announcing RL-Kernel for vime", section "Key Capabilities", first
+ * bullet, and the operator boundary "hidden + lm_head_weight + target_ids ->
+ * selected logprob" in section "Why the Fused Path Wins"):
+ *
+ *   z[t][v]  = h[t] . W[v]                        (bf16 inputs, fp32 accumulation)
+ *   lse[t]   = log sum_{v < V_true} exp(z[t][v])   (columns >= V_true are masked:
+ *              "true vocabulary range", table "Boundary Fixes in the RL-Kernel
+ *              Strict Path", row "Linear logprob", of "vLLM RL-Kernel v0.1.0:
+ *              Bitwise Train-Rollout Consistency on ROCm")
+ *   logp[t]  = z[t][y[t]] - lse[t]
+ *
+ * computed without materialising the [T, V] logits (the fused kernel keeps
+ * running max / sum-exp / target-logit statistics while it walks vocab tiles,
+ * second reason in "Why the Fused Path Wins"). The backward returns dH and dW of
+ * L = sum_t g[t] * logp[t] ("Full-gradient support" bullet), recomputing the
+ * logits tile by tile and forming dz = g * (onehot - softmax).
+ *
+ * Numerical contract (the six observables of "The Numerical Execution
+ * Contract" in the ROCm consistency article, fixed here once for every shape):
+ *  1. Input dependency: logp[t], lse[t] and dH[t] depend only on h[t], y[t], W,
+ *     V_true (and g[t], lse[t] for dH[t]); never on T, on other rows, on the
+ *     stream, on the launch shape or on the GPU's SM count.
+ *  2. Partitioning: the hidden dimension is reduced in steps of 64 (one K=16
+ *     tensor-core instruction at a time, ascending). The vocabulary is cut into
+ *     leaves of RLK_LEAF_WIDTH = 1024 global columns, each walked in 256-column
+ *     tiles in ascending order. No split-K, no atomics.
+ *  3. Merge order: leaves are merged by a balanced pairwise tree defined on
+ *     global leaf indices: nLeaves = ceil(V_true / 1024) leaves are grouped into
+ *     RLK_MAX_SHARDS = 8 super-shards of L = ceil(nLeaves / 8) leaves; inside a
+ *     super-shard the leaves sit in P = next_pow2(L) slots (missing leaves are
+ *     the identity) and are merged pairwise; the 8 super-shard results are then
+ *     merged pairwise (8 -> 4 -> 2 -> 1). Because the tree depends only on V_true,
+ *     a vocab-sharded run (S in {1, 2, 4, 8} contiguous shards, each a
+ *     power-of-two-aligned run of super-shards) followed by rlk_lse_merge gives
+ *     bit-identical logp and lse to the unsharded run.
+ *  4. Precision: bf16 inputs; fp32 accumulation, statistics, logp and lse; dz
+ *     is rounded once to bf16 (it is an operand of the dH/dW products); dH is
+ *     rounded once to bf16 from its fp32 accumulator; dW is fp32.
+ *  5. Rounding: every floating-point step is an explicitly rounded operation
+ *     (round-to-nearest fmul / fadd / fma); nothing is left to compiler contraction.
+ *  6. Primitives: e(x) = ex2.approx.ftz(fma(x, log2 e, -rn(b * log2 e))) for
+ *     exp(x - b) everywhere; log is logf (fp32, CUDA math library).
+ *
+ * Conventions for every entry point:
+ *  - The caller owns every buffer. The library allocates and frees nothing and
+ *    keeps no state between calls (apart from per-device kernel attributes),
+ *    so calls are re-entrant.
+ *  - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) with no host synchronisation. Device pointers must be valid in the
+ *    current CUDA context.
+ *  - Argument errors are returned before anything is launched; T == 0 returns
+ *    RLK_OK and launches nothing (per-token pointers may then be NULL). A
+ *    launch failure returns RLK_ERR_CUDA.
+ *  - Row-major, contiguous tensors. h, W and dz-style bf16 rows need a 16-byte
+ *    aligned base and H % 8 == 0 (tensor-memory-access strides).
+ *  - Targets outside [0, V_true) cannot be checked on the host without a sync:
+ *    their logp is NaN, their gradient row is zero, and RLK_FLAG_BAD_TARGET is
+ *    ORed into *err_flag when err_flag is not NULL.
+ *  - Every internal wait of a kernel is bounded; on expiry the kernel stops,
+ *    ORs RLK_FLAG_TIMEOUT into *err_flag (if given) and the outputs are invalid.
+ */
+#ifndef RLK_H_
+#define RLK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define RLK_API __attribute__((visibility("default")))
+#else
+#define RLK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RLK_OK = 0,
+  RLK_ERR_INVALID_ARG = 1, /* null pointer, negative size, misaligned pointer, H % 8 != 0 */
+  RLK_ERR_UNSUPPORTED = 2, /* a shard split the fixed merge tree cannot express; sizes beyond limits */
+  RLK_ERR_WORKSPACE = 3,   /* workspace missing or smaller than the query returns */
+  RLK_ERR_CUDA = 4         /* a CUDA runtime/driver call failed (launch, tensor-map encode) */
+} rlk_status;
+
+/* bits ORed into *err_flag by the kernels */
+#define RLK_FLAG_BAD_TARGET 1
+#define RLK_FLAG_TIMEOUT 2
+
+/* tiling constants that are part of the numerical contract */
+#define RLK_LEAF_WIDTH 1024
+#define RLK_MAX_SHARDS 8
+
+/* size limits (RLK_ERR_UNSUPPORTED beyond them) */
+#define RLK_MAX_VOCAB (1 << 24)
+#define RLK_MAX_HIDDEN (1 << 16)
+
+/*
+ * Per-token statistics of one vocab shard, natural-log units: m is the largest
+ * logit of the shard's valid columns, s = sum exp(z - m) over them, zt the
+ * target logit if the shard owns y[t], else -inf (NaN for an invalid target).
+ * The identity (empty shard) is {-inf, 0, -inf}. Layout: 12 bytes, no padding.
+ * ("Why the Fused Path Wins", third reason: only statistics cross shards.)
+ */
+typedef struct {
+  float m;
+  float s;
+  float zt;
+} rlk_lse_partial;
+
+/* Bytes of device workspace rlk_linear_logp_fwd needs (256-byte aligned base). */
+RLK_API size_t rlk_linear_logp_fwd_workspace(int64_t T, int64_t H, int64_t V_local);
+
+/*
+ * Forward. The shard holds W rows for global vocab columns
+ * [vocab_start, vocab_start + V_local); the unsharded call is vocab_start = 0,
+ * V_local = V >= V_true.
+ *
+ *   h        device bf16 [T][H]
+ *   W        device bf16 [V_local][H] (this shard's rows)
+ *   y        device int64 [T], global vocab ids
+ *   V_true   global true-vocab bound; columns >= V_true are masked
+ *   logp,lse device fp32 [T] each, or NULL; used when partial == NULL, which
+ *            requires the shard to cover [0, V_true)
+ *   partial  device rlk_lse_partial [T] or NULL: when given, the call writes
+ *            this shard's triple per token instead of logp / lse; combine the
+ *            shards with rlk_lse_merge
+ *   err_flag device int32 or NULL (RLK_FLAG_* bits are ORed in, never cleared)
+ *   workspace, workspace_bytes: device scratch of at least
+ *            rlk_linear_logp_fwd_workspace(T, H, V_local) bytes, 256-byte aligned
+ *
+ * A shard must start at a multiple of the super-shard width
+ * L * RLK_LEAF_WIDTH (L = ceil(ceil(V_true / 1024) / 8)), cover n = ceil(V_local /
+ * (L * 1024)) super-shards with n a power of two and vocab_start / (L * 1024) a
+ * multiple of n, and contain every column of those super-shards below V_true;
+ * otherwise RLK_ERR_UNSUPPORTED.
+ */
+RLK_API rlk_status rlk_linear_logp_fwd(const void* h, const void* W, const int64_t* y, int64_t T,
+                               int64_t H, int64_t V_local, int64_t vocab_start, int64_t V_true,
+                               float* logp, float* lse, rlk_lse_partial* partial,
+                               int32_t* err_flag, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/*
+ * Merge S per-shard triples per token (partials laid out [S][T], shards in
+ * ascending vocab order) by the top levels of the fixed tree, then
+ * lse = m + log(s), logp = zt - lse. S must be 1, 2, 4 or 8. logp, lse: device
+ * fp32 [T]. ("vLLM RL-Kernel v0.1.0 ... on ROCm", "Boundary Fixes" table,
+ * "Linear logprob" row: cross-rank LSE merge; fixed merge order, item 3 of
+ * "The Numerical Execution Contract".)
+ */
+RLK_API rlk_status rlk_lse_merge(const rlk_lse_partial* partials, int32_t S, int64_t T, float* logp,
+                         float* lse, void* stream);
+
+/* Bytes of device workspace rlk_linear_logp_bwd needs: the bf16 dz tile store
+ * [T][round_up(V_local, 256)] (the "controlled workspace" of the fourth reason
+ * in "Why the Fused Path Wins"). */
+RLK_API size_t rlk_linear_logp_bwd_workspace(int64_t T, int64_t H, int64_t V_local);
+
+/*
+ * Backward of L = sum_t g[t] logp[t] for one shard (or the whole vocabulary).
+ *
+ *   h, W, y, T, H, V_local, vocab_start, V_true: as in the forward
+ *   lse      device fp32 [T], the GLOBAL log-sum-exp from the forward / merge
+ *   g        device fp32 [T], upstream gradient
+ *   dH       device [T][H] or NULL: bf16 when dH_fp32_partial == 0, else fp32
+ *            (a shard's partial; sum the shards with rlk_shard_sum_bf16)
+ *   dW       device fp32 [V_local][H] or NULL; rows at or above V_true get 0
+ *   err_flag, workspace, workspace_bytes, stream: as in the forward
+ *
+ * dz[t][v] = g[t] (1[v == y[t]] - exp(z[t][v] - lse[t])) is recomputed from a
+ * fresh z tile with the forward's exact tensor-core sequence, rounded once to
+ * bf16; dH = dz W sums the vocabulary in ascending 64-column steps, dW = dz^T h
+ * sums the tokens in ascending 64-row steps, each output tile by one CTA.
+ */
+RLK_API rlk_status rlk_linear_logp_bwd(const void* h, const void* W, const int64_t* y, const float* lse,
+                               const float* g, int64_t T, int64_t H, int64_t V_local,
+                               int64_t vocab_start, int64_t V_true, void* dH,
+                               int32_t dH_fp32_partial, float* dW, int32_t* err_flag,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * out[i] = bf16(((p[0][i] + p[1][i]) + p[2][i]) + ...), the fixed ascending-order
+ * sum of S fp32 partials laid out [S][n], rounded once to bf16 (RNE). Used to
+ * combine per-shard dH partials. partials, out: device, 16-byte aligned.
+ */
+RLK_API rlk_status rlk_shard_sum_bf16(const float* partials, int32_t S, int64_t n, void* out,
+                              void* stream);
+
+/* Static description of a status code. */
+RLK_API const char* rlk_status_string(rlk_status s);
+
+/* Library version string, e.g. "rlk 0.1.0 sm_103a". */
+RLK_API const char* rlk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RLK_H_ */
