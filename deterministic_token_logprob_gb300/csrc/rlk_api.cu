@@ -296,7 +296,7 @@ rlk_status rlk_linear_logp_fwd(const void* h, const void* W, const int64_t* y, i
                                void* stream) {
   rlk_status st = common_checks(h, W, y, T, H, V_local, vocab_start, V_true);
   if (st != RLK_OK) return st;
-  if (!partial && !logp && !lse) return RLK_ERR_INVALID_ARG;
+  if (T > 0 && !partial && !logp && !lse) return RLK_ERR_INVALID_ARG;
   ShardGeom g;
   st = shard_geometry(V_local, vocab_start, V_true, &g);
   if (st != RLK_OK) return st;

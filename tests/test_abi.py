@@ -95,6 +95,7 @@ def test_forward_argument_errors(lib):
 def test_forward_empty_and_workspace(lib):
     assert fwd(lib, T=0) == OK
     assert fwd(lib, T=0, h=None, y=None) == OK        # an empty batch has no storage
+    assert fwd(lib, T=0, h=None, y=None, logp=None, lse=None) == OK
     assert fwd(lib, T=0, W=None) == INVALID
     assert fwd(lib, T=0, h=FAKE, ws=None, ws_bytes=0) == OK
     need = lib.rlk_linear_logp_fwd_workspace(4, 64, 4096)
