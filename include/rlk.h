@@ -191,6 +191,32 @@ RLK_API rlk_status rlk_linear_logp_bwd(const void* h, const void* W, const int64
 RLK_API rlk_status rlk_shard_sum_bf16(const float* partials, int32_t S, int64_t n, void* out,
                               void* stream);
 
+/*
+ * Forward without a workspace argument, for callers that cannot allocate device
+ * memory: runtimes whose device memory is fully reserved up front by another
+ * allocator (a serving engine that pre-plans every buffer), or latency-critical
+ * loops where cudaMalloc / cudaFree would synchronise the device and stall the
+ * other streams. The pages have no counterpart to this entry point.
+ *
+ * Same arguments, results and errors as rlk_linear_logp_fwd, minus workspace and
+ * workspace_bytes. The scratch it needs instead is one static device array of
+ * RLK_FWD_NOALLOC_SCRATCH_BYTES (16 MiB), held by every GPU that loads the library
+ * until the process exits; the call itself allocates nothing. A shape whose
+ * rlk_linear_logp_fwd_workspace(T, H, V_local) exceeds that size is rejected with
+ * RLK_ERR_WORKSPACE before anything runs (e.g. at most 9383 tokens for a 151936-row
+ * W). The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture. All calls on a
+ * device share the array: calls that can overlap on the GPU (different streams with
+ * no ordering between them) race and give wrong results.
+ */
+#define RLK_FWD_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+RLK_API rlk_status rlk_linear_logp_fwd_noalloc(const void* h, const void* W, const int64_t* y,
+                                               int64_t T, int64_t H, int64_t V_local,
+                                               int64_t vocab_start, int64_t V_true, float* logp,
+                                               float* lse, rlk_lse_partial* partial,
+                                               int32_t* err_flag, void* stream);
+
 /* Static description of a status code. */
 RLK_API const char* rlk_status_string(rlk_status s);
 
