@@ -175,7 +175,7 @@ def config_dict(w: workloads.Workload, world: int):
 class Path:
     """Device buffers and the C-ABI calls of one step."""
 
-    def __init__(self, rlk, torch, w: workloads.Workload, d: dict, device):
+    def __init__(self, rlk, torch, w: workloads.Workload, d: dict, device, with_dW: bool = True):
         self.rlk, self.torch, self.w = rlk, torch, w
         bf = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)  # noqa: E731
         self.h = bf(d["h"])
@@ -186,7 +186,7 @@ class Path:
         f32 = torch.float32
         self.logp = torch.empty(T, dtype=f32, device=device)
         self.lse = torch.empty(T, dtype=f32, device=device)
-        self.dW = torch.empty((V, H), dtype=f32, device=device)
+        self.dW = torch.empty((V, H), dtype=f32, device=device) if with_dW else None
         shards = w.shards or ((0, V),)
         self.shards = shards
         self.fws = torch.empty(max(rlk.fwd_workspace_bytes(T, H, n) for _, n in shards),
@@ -390,6 +390,50 @@ def e2e(rlk, torch, path, w, d, device, args):
             "d2h_bytes_per_step": d2h, "ms_per_step": ms}
 
 
+def run_case(args):
+    """One stage of the path at the Qwen3-8B H and V with --tokens tokens, timed per call
+    with CUDA events (for per-kernel timing and small-case ncu captures)."""
+    import torch
+
+    import deterministic_token_logprob_gb300 as rlk
+    from deterministic_token_logprob_gb300 import build as libbuild
+    libbuild.build()
+    base = workloads.QWEN3_8B
+    V = args.vocab or base.V
+    V_true = V - (base.V - base.V_true) if V > base.V - base.V_true else V
+    w = workloads.Workload(f"case_{args.case}", T=args.tokens, H=base.H, V=V, V_true=V_true,
+                           g_kind="grpo")
+    d = workloads.make_inputs(w)
+    dev = torch.device("cuda", 0)
+    path = Path(rlk, torch, w, d, dev, with_dW=args.case == "dw")
+    path.forward()
+    if args.case == "fwd":
+        call = path.forward
+    else:
+        want_dH, want_dW = args.case == "dh", args.case == "dw"
+
+        def call():
+            rlk.linear_logp_bwd(path.h, path.W, path.y, path.lse, path.g, w.V_true,
+                                out=(path.dH if want_dH else None, path.dW if want_dW else None),
+                                want_dH=want_dH, want_dW=want_dW, workspace=path.bws)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    ms = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        torch.cuda.synchronize(dev)
+        ms.append(a.elapsed_time(b))
+    flops = 2.0 * w.T * w.H * w.V_true * (1 if args.case in ("fwd", "dz") else 2)
+    print(json.dumps({"case": args.case, "T": w.T, "H": w.H, "V": w.V, "V_true": w.V_true,
+                      "ms": ms, "tflops_best": flops / (min(ms) / 1e3) / 1e12,
+                      "kernels_per_call": {"fwd": 2, "dz": 1, "dh": 2, "dw": 2}[args.case]}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -398,9 +442,17 @@ def main():
     ap.add_argument("--impl", choices=["rlk", "reference"], default="rlk")
     ap.add_argument("--workload", choices=["qwen3_8b", "qwen3_30b_tp2", "tiny"], default="qwen3_8b")
     ap.add_argument("--quick", action="store_true", help="skip the forward-only, e2e and CPU legs")
+    ap.add_argument("--case", choices=["fwd", "dz", "dh", "dw"], default=None,
+                    help="time one stage only (dz alone; dh / dw each after its dz)")
+    ap.add_argument("--tokens", type=int, default=1024, help="tokens for --case")
+    ap.add_argument("--vocab", type=int, default=0,
+                    help="vocab rows for --case (default 151936; V_true = V - 267)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.case:
+        run_case(args)
+        return
     w = workloads.CONFIGS[args.workload]
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
