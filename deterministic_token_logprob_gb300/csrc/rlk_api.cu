@@ -198,12 +198,6 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
   return r == CUDA_SUCCESS;
 }
 
-bool sm_count(int* n) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  return cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && *n > 0;
-}
-
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -313,29 +307,26 @@ rlk_status rlk_linear_logp_fwd(const void* h, const void* W, const int64_t* y, i
   float* ws_zt = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * arr);
 
   if (g.n_leaves_local > 0) {
-    int n_sm = 0;
-    if (!sm_count(&n_sm)) return RLK_ERR_CUDA;
     CUtensorMap tmA, tmB;
     if (!encode_2d(&tmA, h, H, T, H, 64, BM)) return RLK_ERR_CUDA;
-    if (!encode_2d(&tmB, W, H, V_local, H, 64, BN)) return RLK_ERR_CUDA;
+    if (!encode_2d(&tmB, W, H, V_local, H, 64, B_HALF)) return RLK_ERR_CUDA;
     GemmArgs a;
     a.T = static_cast<int32_t>(T);
     a.H = static_cast<int32_t>(H);
     a.V_local = static_cast<int32_t>(V_local);
     a.vocab_start = static_cast<int32_t>(vocab_start);
     a.V_true = static_cast<int32_t>(V_true);
-    a.n_tt = static_cast<int32_t>(ceil_div(T, BM));
+    a.n_pm = static_cast<int32_t>(ceil_div(T, PAIR_M));
     a.leaf0 = static_cast<int32_t>(g.leaf0);
     a.n_leaves = static_cast<int32_t>(g.n_leaves_local);
-    a.n_items = a.n_tt * a.n_leaves;
+    a.n_items = a.n_pm * a.n_leaves;
     a.n_kb = static_cast<int32_t>(ceil_div(H, BK));
     a.y = y;
     a.ws_m = ws_m;
     a.ws_s = ws_s;
     a.ws_zt = ws_zt;
     a.err_flag = err_flag;
-    const int grid = static_cast<int>(std::min<int64_t>(a.n_items, n_sm));
-    if (launch_gemm_fwd(tmA, tmB, a, grid, s) != cudaSuccess) return RLK_ERR_CUDA;
+    if (launch_gemm_fwd(tmA, tmB, a, s) != cudaSuccess) return RLK_ERR_CUDA;
   }
 
   TreeArgs ta;
@@ -394,24 +385,22 @@ rlk_status rlk_linear_logp_bwd(const void* h, const void* W, const int64_t* y, c
   if (workspace_bytes < rlk_linear_logp_bwd_workspace(T, H, V_local)) return RLK_ERR_WORKSPACE;
   if (Vd > INT32_MAX / 2) return RLK_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int n_sm = 0;
-  if (!sm_count(&n_sm)) return RLK_ERR_CUDA;
   uint16_t* dz = static_cast<uint16_t*>(workspace);
-  const int32_t n_tt = static_cast<int32_t>(ceil_div(T, BM));
+  const int32_t n_pm = static_cast<int32_t>(ceil_div(T, PAIR_M));
 
   // 1. recompute z tiles -> dz (bf16) workspace
   {
     CUtensorMap tmA, tmB;
     if (!encode_2d(&tmA, h, H, T, H, 64, BM)) return RLK_ERR_CUDA;
-    if (!encode_2d(&tmB, W, H, V_local, H, 64, BN)) return RLK_ERR_CUDA;
+    if (!encode_2d(&tmB, W, H, V_local, H, 64, B_HALF)) return RLK_ERR_CUDA;
     GemmArgs a;
     a.T = static_cast<int32_t>(T);
     a.H = static_cast<int32_t>(H);
     a.V_local = static_cast<int32_t>(V_local);
     a.vocab_start = static_cast<int32_t>(vocab_start);
     a.V_true = static_cast<int32_t>(V_true);
-    a.n_tt = n_tt;
-    a.n_items = static_cast<int32_t>(Vd / BN) * n_tt;
+    a.n_pm = n_pm;
+    a.n_items = static_cast<int32_t>(Vd / BN) * n_pm;
     a.n_kb = static_cast<int32_t>(ceil_div(H, BK));
     a.y = y;
     a.lse = lse;
@@ -419,8 +408,7 @@ rlk_status rlk_linear_logp_bwd(const void* h, const void* W, const int64_t* y, c
     a.dz = dz;
     a.dz_ld = Vd;
     a.err_flag = err_flag;
-    const int grid = static_cast<int>(std::min<int64_t>(a.n_items, n_sm));
-    if (launch_gemm_dz(tmA, tmB, a, grid, s) != cudaSuccess) return RLK_ERR_CUDA;
+    if (launch_gemm_dz(tmA, tmB, a, s) != cudaSuccess) return RLK_ERR_CUDA;
   }
 
   // 2. dH = dz W over this shard's valid columns
@@ -436,7 +424,7 @@ rlk_status rlk_linear_logp_bwd(const void* h, const void* W, const int64_t* y, c
       GemmArgs a;
       a.T = static_cast<int32_t>(T);
       a.H = static_cast<int32_t>(H);
-      a.n_mt = n_tt;
+      a.n_mt = n_pm;
       a.n_nt = static_cast<int32_t>(ceil_div(H, BN));
       a.n_items = a.n_mt * a.n_nt;
       a.n_kb = static_cast<int32_t>(ceil_div(V_valid, BK));
@@ -446,8 +434,7 @@ rlk_status rlk_linear_logp_bwd(const void* h, const void* W, const int64_t* y, c
       a.out_cols = static_cast<int32_t>(H);
       a.out_f32 = dH_fp32_partial ? 1 : 0;
       a.err_flag = err_flag;
-      const int grid = static_cast<int>(std::min<int64_t>(a.n_items, n_sm));
-      if (launch_gemm_dh(tmA, tmB, a, grid, s) != cudaSuccess) return RLK_ERR_CUDA;
+      if (launch_gemm_dh(tmA, tmB, a, s) != cudaSuccess) return RLK_ERR_CUDA;
     }
   }
 
@@ -459,7 +446,7 @@ rlk_status rlk_linear_logp_bwd(const void* h, const void* W, const int64_t* y, c
     GemmArgs a;
     a.T = static_cast<int32_t>(T);
     a.H = static_cast<int32_t>(H);
-    a.n_mt = static_cast<int32_t>(ceil_div(V_local, BM));
+    a.n_mt = static_cast<int32_t>(ceil_div(V_local, PAIR_M));
     a.n_nt = static_cast<int32_t>(ceil_div(H, BN));
     a.n_items = a.n_mt * a.n_nt;
     a.n_kb = static_cast<int32_t>(ceil_div(T, BK));
@@ -469,8 +456,7 @@ rlk_status rlk_linear_logp_bwd(const void* h, const void* W, const int64_t* y, c
     a.out_cols = static_cast<int32_t>(H);
     a.out_f32 = 1;
     a.err_flag = err_flag;
-    const int grid = static_cast<int>(std::min<int64_t>(a.n_items, n_sm));
-    if (launch_gemm_dw(tmA, tmB, a, grid, s) != cudaSuccess) return RLK_ERR_CUDA;
+    if (launch_gemm_dw(tmA, tmB, a, s) != cudaSuccess) return RLK_ERR_CUDA;
   }
   return RLK_OK;
 }

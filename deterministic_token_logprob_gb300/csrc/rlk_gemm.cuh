@@ -12,17 +12,22 @@
 //   MODE_DH   dH = dz W    (K = vocab, ascending), bf16 or fp32 output.
 //   MODE_DW   dW = dz^T h  (K = tokens, ascending), fp32 output.
 //
-// Kernel structure (one persistent CTA per SM, 192 threads):
-//   warp 0     TMA producer: 4-stage shared-memory ring of 48 KiB stages
-//              (A 128x64 + B 256x64 bf16, 128-byte swizzle)
-//   warp 1     allocates 512 TMEM columns; one thread issues tcgen05.mma
-//              (M=128, N=256, K=16; four per stage) into one of two fp32
-//              accumulators, releasing stages and accumulators by tcgen05.commit
-//   warps 2-5  epilogue: tcgen05.ld (thread = token row, lane quarter = warp % 4)
-//              -> registers -> mode-specific math -> global memory
-// Work items are assigned statically (item = blockIdx.x + i * gridDim.x), so
-// numerics never depend on the grid: each output element is produced by one
-// fixed instruction sequence regardless of T, batch composition or SM count.
+// Kernel structure: clusters of two CTAs (one per SM, persistent) compute
+// 256 x 256 tiles with tcgen05 cta_group::2. Per CTA, 192 threads:
+//   warp 0     TMA producer: 6-stage shared-memory ring of 32 KiB stages (this
+//              CTA's 128 x 64 slice of A and 128 x 64 slice of B, 128-byte
+//              swizzle). Both CTAs' copies signal the even CTA's "full" barriers.
+//   warp 1     allocates 512 TMEM columns in both CTAs (two fp32 accumulators of
+//              128 rows x 256 columns each); in the even CTA one thread issues
+//              tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16; four per stage)
+//              and releases stages / publishes accumulators in BOTH CTAs with
+//              multicast tcgen05.commit.
+//   warps 2-5  epilogue in each CTA: tcgen05.ld of its own 128 accumulator rows
+//              (thread = row, lane quarter = warp % 4) -> registers -> mode math ->
+//              global memory; releases the accumulator on the even CTA's barrier.
+// Work items are assigned statically (item = cluster + i * clusters), so numerics
+// never depend on the grid: each output element is produced by one fixed
+// instruction sequence regardless of T, batch composition or SM count.
 #pragma once
 
 #include "rlk_internal.h"
@@ -34,14 +39,14 @@ template <int MODE>
 struct Operands {
   static constexpr bool A_MN = (MODE == MODE_DW);
   static constexpr bool B_MN = (MODE == MODE_DH || MODE == MODE_DW);
-  static constexpr uint32_t IDESC = make_idesc_bf16(BM, BN, A_MN, B_MN);
+  static constexpr uint32_t IDESC = make_idesc_bf16(PAIR_M, BN, A_MN, B_MN);
 };
 
 // Number of 256-wide tiles in a work item.
 template <int MODE>
 __device__ __forceinline__ int item_tiles(const GemmArgs& a, int item) {
   if constexpr (MODE == MODE_FWD) {
-    const int leaf_local = item / a.n_tt;
+    const int leaf_local = item / a.n_pm;
     const int col0 = (a.leaf0 + leaf_local) * LEAF;
     const int end = min(col0 + LEAF, a.V_true);
     return (end - col0 + BN - 1) / BN;
@@ -50,23 +55,39 @@ __device__ __forceinline__ int item_tiles(const GemmArgs& a, int item) {
   }
 }
 
-// Tile origin: m0 = first row of the A operand's M extent, n0 = first row of
-// the B operand's N extent (fwd/dz: local W row; dH/dW: output column).
+// Pair-tile origin: m0 = first of the pair's 256 A / accumulator rows, n0 = first
+// of its 256 B rows (fwd/dz: local W row; dH/dW: output column).
 template <int MODE>
 __device__ __forceinline__ void tile_origin(const GemmArgs& a, int item, int j, int& m0, int& n0) {
   if constexpr (MODE == MODE_FWD) {
-    const int leaf_local = item / a.n_tt, tt = item % a.n_tt;
-    m0 = tt * BM;
+    const int leaf_local = item / a.n_pm, pm = item % a.n_pm;
+    m0 = pm * PAIR_M;
     n0 = (a.leaf0 + leaf_local) * LEAF + j * BN - a.vocab_start;
   } else if constexpr (MODE == MODE_DZ) {
-    const int vt = item / a.n_tt, tt = item % a.n_tt;
-    m0 = tt * BM;
+    const int vt = item / a.n_pm, pm = item % a.n_pm;
+    m0 = pm * PAIR_M;
     n0 = vt * BN;
   } else {
     const int mt = item / a.n_nt, nt = item % a.n_nt;
-    m0 = mt * BM;
+    m0 = mt * PAIR_M;
     n0 = nt * BN;
   }
+}
+
+// Shared state of one CTA of the pair.
+struct PairCtx {
+  uint32_t rank;           // 0 = even CTA (issues the MMAs), 1 = odd CTA
+  uint32_t cluster;        // cluster index
+  uint32_t n_clusters;
+  volatile int* abort_flag;
+  uint32_t peer_abort;     // shared::cluster address of the peer CTA's abort flag
+};
+
+// Bounded wait; on expiry it also raises the peer CTA's abort flag.
+__device__ __forceinline__ bool pair_wait(uint64_t* bar, uint32_t parity, const PairCtx& c) {
+  if (mbar_wait_bounded(bar, parity, c.abort_flag)) return true;
+  st_cluster_u32(c.peer_abort, 1u);
+  return false;
 }
 
 // A wait that ignores the abort flag (used only to drain work already in flight).
@@ -79,80 +100,98 @@ __device__ __forceinline__ bool mbar_wait_timeout(uint64_t* bar, uint32_t parity
   return true;
 }
 
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (global_timer_ns() - t0 < ns) {
+  }
+}
+
 // ---------------------------------------------------------------------------
-// warp 0: TMA producer (one thread)
+// warp 0: TMA producer (one thread per CTA)
 // ---------------------------------------------------------------------------
 template <int MODE>
 __device__ void producer_loop(const CUtensorMap* tmA, const CUtensorMap* tmB, const GemmArgs& a,
-                              uint8_t* smem, uint64_t* full, uint64_t* empty,
-                              volatile int* abort_flag) {
+                              uint8_t* smem, uint64_t* full, uint64_t* empty, const PairCtx& c) {
+  // L2 policy per operand: h is re-read by every leaf / vocab tile (fwd, dz) or by
+  // every vocab tile of dW, so it is kept; everything else is normal.
+  const uint64_t pol_keep = policy_evict_last();
+  const uint64_t pol_norm = policy_evict_normal();
+  const uint64_t polA = (MODE == MODE_FWD || MODE == MODE_DZ) ? pol_keep : pol_norm;
+  const uint64_t polB = (MODE == MODE_DW) ? pol_keep : pol_norm;
+  const uint32_t r = c.rank;
   uint32_t issued = 0;
   bool ok = true;
-  for (int item = blockIdx.x; ok && item < a.n_items; item += gridDim.x) {
+  for (int item = c.cluster; ok && item < a.n_items; item += c.n_clusters) {
     const int ntiles = item_tiles<MODE>(a, item);
     for (int j = 0; ok && j < ntiles; ++j) {
       int m0, n0;
       tile_origin<MODE>(a, item, j, m0, n0);
+      const int am = m0 + r * BM;      // this CTA's A rows
+      const int bn = n0 + r * B_HALF;  // this CTA's B rows
       for (int kb = 0; kb < a.n_kb; ++kb) {
         const uint32_t s = issued % STAGES, ph = (issued / STAGES) & 1u;
-        if (!mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) {
+        if (!pair_wait(&empty[s], ph ^ 1u, c)) {
           ok = false;
           break;
         }
         uint8_t* sA = smem + s * STAGE_BYTES;
         uint8_t* sB = sA + A_STAGE_BYTES;
-        mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+        const uint32_t bar = map_to_cta(smem_u32(&full[s]), 0);  // the even CTA's barrier
+        if (r == 0) mbar_arrive_expect_tx(&full[s], PAIR * STAGE_BYTES);
         const int k0 = kb * BK;
         if constexpr (MODE == MODE_FWD || MODE == MODE_DZ) {
-          tma_load_2d(sA, tmA, &full[s], k0, m0);  // h rows m0.., K-major box 64 x 128
-          tma_load_2d(sB, tmB, &full[s], k0, n0);  // W rows n0.., K-major box 64 x 256
+          tma_load_2d_pair(sA, tmA, bar, k0, am, polA);   // h, K-major box 64 x 128
+          tma_load_2d_pair(sB, tmB, bar, k0, bn, polB);   // W, K-major box 64 x 128
         } else if constexpr (MODE == MODE_DH) {
-          tma_load_2d(sA, tmA, &full[s], k0, m0);  // dz rows m0.., K-major box 64 x 128
+          tma_load_2d_pair(sA, tmA, bar, k0, am, polA);   // dz, K-major box 64 x 128
 #pragma unroll
-          for (int q = 0; q < BN / 64; ++q)        // W[k0.., n0+64q..] MN-major boxes 64 x 64
-            tma_load_2d(sB + q * MN_ATOM_BYTES, tmB, &full[s], n0 + q * 64, k0);
+          for (int q = 0; q < B_HALF / 64; ++q)           // W[k0.., bn+64q..], MN-major 64 x 64
+            tma_load_2d_pair(sB + q * MN_ATOM_BYTES, tmB, bar, bn + q * 64, k0, polB);
         } else {
 #pragma unroll
-          for (int q = 0; q < BM / 64; ++q)        // dz[k0.., m0+64q..] MN-major boxes 64 x 64
-            tma_load_2d(sA + q * MN_ATOM_BYTES, tmA, &full[s], m0 + q * 64, k0);
+          for (int q = 0; q < BM / 64; ++q)               // dz[k0.., am+64q..], MN-major 64 x 64
+            tma_load_2d_pair(sA + q * MN_ATOM_BYTES, tmA, bar, am + q * 64, k0, polA);
 #pragma unroll
-          for (int q = 0; q < BN / 64; ++q)        // h[k0.., n0+64q..] MN-major boxes 64 x 64
-            tma_load_2d(sB + q * MN_ATOM_BYTES, tmB, &full[s], n0 + q * 64, k0);
+          for (int q = 0; q < B_HALF / 64; ++q)           // h[k0.., bn+64q..], MN-major 64 x 64
+            tma_load_2d_pair(sB + q * MN_ATOM_BYTES, tmB, bar, bn + q * 64, k0, polB);
         }
         ++issued;
       }
     }
   }
   if (ok) {
-    // Tail: every stage must have been released by the MMA warp (all its
-    // commits have landed) before the CTA may exit.
+    // Tail: every stage must have been released by the MMAs (their multicast
+    // commits have landed here) before the CTA may exit.
     for (uint32_t i = 0; i < STAGES; ++i) {
       const uint32_t it = issued + i;
-      if (!mbar_wait_bounded(&empty[it % STAGES], ((it / STAGES) & 1u) ^ 1u, abort_flag)) break;
+      if (!pair_wait(&empty[it % STAGES], ((it / STAGES) & 1u) ^ 1u, c)) break;
     }
-  } else {
-    // Abort: wait for the copies already in flight so no TMA write lands after exit.
+  } else if (c.rank == 0) {
+    // Abort: wait for the copies already in flight (the even CTA's full barriers
+    // also count the odd CTA's bytes) so no TMA write lands after exit.
     const uint32_t first = issued > STAGES ? issued - STAGES : 0;
     for (uint32_t it = first; it < issued; ++it)
       mbar_wait_timeout(&full[it % STAGES], (it / STAGES) & 1u);
+  } else {
+    spin_ns(1000000);  // odd CTA: its copies signal the peer; give them 1 ms to land
   }
 }
 
 // ---------------------------------------------------------------------------
-// warp 1: tcgen05.mma issuer (one thread)
+// warp 1 of the even CTA: tcgen05.mma issuer (one thread)
 // ---------------------------------------------------------------------------
 template <int MODE>
 __device__ void mma_loop(const GemmArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
                          uint64_t* acc_full, uint64_t* acc_empty, uint64_t* drain,
-                         uint32_t tmem_base, volatile int* abort_flag) {
+                         uint32_t tmem_base, const PairCtx& c) {
   using Ops = Operands<MODE>;
   uint32_t it = 0, tile = 0;
   bool ok = true;
-  for (int item = blockIdx.x; ok && item < a.n_items; item += gridDim.x) {
+  for (int item = c.cluster; ok && item < a.n_items; item += c.n_clusters) {
     const int ntiles = item_tiles<MODE>(a, item);
     for (int j = 0; ok && j < ntiles; ++j) {
       const uint32_t buf = tile & 1u, use = tile >> 1;
-      if (!mbar_wait_bounded(&acc_empty[buf], (use & 1u) ^ 1u, abort_flag)) {
+      if (!pair_wait(&acc_empty[buf], (use & 1u) ^ 1u, c)) {
         ok = false;
         break;
       }
@@ -160,7 +199,7 @@ __device__ void mma_loop(const GemmArgs& a, uint8_t* smem, uint64_t* full, uint6
       const uint32_t d_tmem = tmem_base + buf * BN;
       for (int kb = 0; kb < a.n_kb; ++kb, ++it) {
         const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-        if (!mbar_wait_bounded(&full[s], ph, abort_flag)) {
+        if (!pair_wait(&full[s], ph, c)) {
           ok = false;
           break;
         }
@@ -173,22 +212,22 @@ __device__ void mma_loop(const GemmArgs& a, uint8_t* smem, uint64_t* full, uint6
                                         : make_smem_desc(a_base + k * 32, 16, 1024);
           const uint64_t bd = Ops::B_MN ? make_smem_desc(b_base + k * 2048, MN_ATOM_BYTES, 1024)
                                         : make_smem_desc(b_base + k * 32, 16, 1024);
-          umma_bf16(d_tmem, ad, bd, Ops::IDESC, (kb | k) != 0 ? 1u : 0u);
+          umma_bf16_pair(d_tmem, ad, bd, Ops::IDESC, (kb | k) != 0 ? 1u : 0u);
         }
-        umma_commit(&empty[s]);  // stage s is free once these MMAs have read it
+        umma_commit_pair_multicast(&empty[s], 0x3);  // stage s free in both CTAs
       }
       if (!ok) break;
-      umma_commit(&acc_full[buf]);  // accumulator complete
+      umma_commit_pair_multicast(&acc_full[buf], 0x3);  // accumulator complete in both CTAs
       ++tile;
     }
   }
   // Every issued MMA must have finished before TMEM is released.
-  umma_commit(drain);
+  umma_commit_pair_local(drain);
   mbar_wait_timeout(drain, 0);
 }
 
 // ---------------------------------------------------------------------------
-// warps 2-5: epilogues (128 threads; thread = one accumulator row)
+// warps 2-5: epilogues (128 threads per CTA; thread = one accumulator row)
 // ---------------------------------------------------------------------------
 
 __device__ __forceinline__ float max64(const float (&v)[64]) {
@@ -243,17 +282,27 @@ __device__ __forceinline__ void fwd_chunk(float (&v)[64], int valid, int tl, Row
   st.s = __fadd_rn(st.s, sum_exp64(v, st.nb));
 }
 
+__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
+  uint4 w;
+  w.x = pack_bf16x2(v[0], v[1]);
+  w.y = pack_bf16x2(v[2], v[3]);
+  w.z = pack_bf16x2(v[4], v[5]);
+  w.w = pack_bf16x2(v[6], v[7]);
+  return w;
+}
+
 template <int MODE>
 __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* acc_empty,
-                              uint32_t tmem_base, volatile int* abort_flag) {
+                              uint32_t tmem_base, const PairCtx& c) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;  // TMEM lane quarter this warp may access
   const int row = quarter * 32 + lane;
   const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+  const uint64_t pol_out = policy_evict_first();  // outputs are streamed, never re-read here
   uint32_t tile = 0;
   bool ok = true;
 
-  for (int item = blockIdx.x; ok && item < a.n_items; item += gridDim.x) {
+  for (int item = c.cluster; ok && item < a.n_items; item += c.n_clusters) {
     const int ntiles = item_tiles<MODE>(a, item);
     int m0, n0;
     tile_origin<MODE>(a, item, 0, m0, n0);
@@ -263,7 +312,7 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
     int64_t yt = -1;
     float g_t = 0.f, nl = 0.f;
     bool yvalid = false;
-    const int t = m0 + row;  // token row (fwd, dz, dH) or vocab row (dW)
+    const int t = m0 + static_cast<int>(c.rank) * BM + row;  // token row (fwd, dz, dH) or vocab row (dW)
     if constexpr (MODE == MODE_FWD) {
       if (t < a.T) yt = a.y[t];
     } else if constexpr (MODE == MODE_DZ) {
@@ -278,7 +327,7 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
 
     for (int j = 0; j < ntiles; ++j) {
       const uint32_t buf = tile & 1u, use = tile >> 1;
-      bool got = mbar_wait_bounded(&acc_full[buf], use & 1u, abort_flag);
+      bool got = pair_wait(&acc_full[buf], use & 1u, c);
       got = __all_sync(0xffffffffu, got);
       if (!got) {
         ok = false;
@@ -330,16 +379,8 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
               if (i >= valid) v[i] = 0.f;
           }
           if (t < a.T) {
-            uint4* p = reinterpret_cast<uint4*>(dst + ch);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              uint4 w;
-              w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-              w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-              w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-              w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-              p[q] = w;
-            }
+            for (int q = 0; q < 8; ++q) st_global_v4_hint(dst + ch + 8 * q, pack8_bf16(v + 8 * q), pol_out);
           }
         }
       } else {
@@ -356,20 +397,15 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
 #pragma unroll
               for (int q = 0; q < 16; ++q)
                 if (col + 4 * q < a.out_cols)
-                  *reinterpret_cast<float4*>(p + 4 * q) =
-                      make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                  st_global_v4_hint(p + 4 * q,
+                                    make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
+                                               __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3])),
+                                    pol_out);
             } else {
               uint16_t* p = static_cast<uint16_t*>(a.out) + static_cast<size_t>(t) * a.out_ld + col;
 #pragma unroll
               for (int q = 0; q < 8; ++q)
-                if (col + 8 * q < a.out_cols) {
-                  uint4 w;
-                  w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-                  w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-                  w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-                  w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-                  *reinterpret_cast<uint4*>(p + 8 * q) = w;
-                }
+                if (col + 8 * q < a.out_cols) st_global_v4_hint(p + 8 * q, pack8_bf16(v + 8 * q), pol_out);
             }
           }
         }
@@ -377,13 +413,13 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
 
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&acc_empty[buf]), 0));
       ++tile;
     }
 
     if constexpr (MODE == MODE_FWD) {
       if (ok && t < a.T) {
-        const int leaf_local = item / a.n_tt;
+        const int leaf_local = item / a.n_pm;
         const size_t o = static_cast<size_t>(leaf_local) * a.T + t;
         a.ws_m[o] = st.m;
         a.ws_s[o] = st.s;
@@ -394,7 +430,7 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
 }
 
 // ---------------------------------------------------------------------------
-// the kernel
+// the kernel (launched as clusters of 2 CTAs)
 // ---------------------------------------------------------------------------
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -409,20 +445,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* abort_word = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  PairCtx c;
+  c.rank = cluster_ctarank();
+  c.cluster = blockIdx.x / PAIR;
+  c.n_clusters = gridDim.x / PAIR;
+  c.abort_flag = abort_word;
+  c.peer_abort = map_to_cta(smem_u32(abort_word), c.rank ^ 1u);
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&full[s], 1);   // used in the even CTA: its producer's expect_tx arrival
+      mbar_init(&empty[s], 1);  // one multicast commit per use
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+      mbar_init(&acc_empty[b], PAIR * 4);  // one arrival per epilogue warp of both CTAs
     }
     mbar_init(drain, 1);
-    *abort_flag = 0;
+    *abort_word = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -430,40 +473,70 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any cross-CTA arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) producer_loop<MODE>(&tmA, &tmB, a, smem, full, empty, abort_flag);
+    if (lane == 0) producer_loop<MODE>(&tmA, &tmB, a, smem, full, empty, c);
   } else if (warp == 1) {
-    if (lane == 0)
-      mma_loop<MODE>(a, smem, full, empty, acc_full, acc_empty, drain, tmem_base, abort_flag);
+    if (lane == 0 && c.rank == 0)
+      mma_loop<MODE>(a, smem, full, empty, acc_full, acc_empty, drain, tmem_base, c);
   } else {
-    epilogue_loop<MODE>(a, acc_full, acc_empty, tmem_base, abort_flag);
+    epilogue_loop<MODE>(a, acc_full, acc_empty, tmem_base, c);
   }
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // all MMAs of the pair drained, all cross-CTA arrivals done
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
-  if (threadIdx.x == 0 && *abort_flag && a.err_flag) atomicOr(a.err_flag, 2);
+  if (threadIdx.x == 0 && *c.abort_flag && a.err_flag) atomicOr(a.err_flag, 2);
+  cluster_sync();  // neither CTA exits while its peer may still address its shared memory
 }
 
 template <int MODE>
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                        int grid, cudaStream_t stream) {
+                        cudaStream_t stream) {
   auto kernel = gemm_kernel<MODE>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(tmA, tmB, a);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = PAIR;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // Resident pairs of this kernel on the current device (queried once per device).
+  static int resident[64] = {};
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int clusters = dev < 64 ? resident[dev] : 0;
+  if (clusters <= 0) {
+    cfg.gridDim = dim3(PAIR, 1, 1);
+    e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters <= 0) return cudaErrorInvalidConfiguration;
+    if (dev < 64) resident[dev] = clusters;
+  }
+  clusters = min(clusters, a.n_items);
+  cfg.gridDim = dim3(PAIR * clusters, 1, 1);
+  e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -4,8 +4,8 @@
 namespace rlk {
 
 cudaError_t launch_gemm_dw(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                           int grid, cudaStream_t stream) {
-  return launch_gemm<MODE_DW>(tmA, tmB, a, grid, stream);
+                           cudaStream_t stream) {
+  return launch_gemm<MODE_DW>(tmA, tmB, a, stream);
 }
 
 }  // namespace rlk

@@ -18,13 +18,19 @@ constexpr int LEAF = 1024;   // vocab columns per leaf of the merge tree
 constexpr int TILES_PER_LEAF = LEAF / BN;
 constexpr int MAX_SHARDS = 8;
 
-constexpr int STAGES = 4;
-constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KiB
-constexpr int B_STAGE_BYTES = BN * BK * 2;  // 32 KiB
+// A CTA pair (cluster of 2, tcgen05 cta_group::2) computes one 256 x 256 tile: CTA r
+// holds rows [128 r, 128 r + 128) of A and of the accumulator, and rows
+// [128 r, 128 r + 128) of the 256-row B tile.
+constexpr int PAIR = 2;
+constexpr int PAIR_M = BM * PAIR;           // 256 accumulator rows per pair
+constexpr int B_HALF = BN / PAIR;           // 128 B rows per CTA
+constexpr int STAGES = 6;
+constexpr int A_STAGE_BYTES = BM * BK * 2;      // 16 KiB
+constexpr int B_STAGE_BYTES = B_HALF * BK * 2;  // 16 KiB
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int MN_ATOM_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) TMA box, 8 KiB
 constexpr int NUM_THREADS = 192;            // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int TMEM_COLS = 512;              // two fp32 128x256 accumulators
+constexpr int TMEM_COLS = 512;              // two fp32 128x256 accumulators per CTA
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /* alignment slack */ + 256 /* barriers */;
 
 enum GemmMode : int {
@@ -41,7 +47,7 @@ struct GemmArgs {
   int32_t* err_flag = nullptr;
   // forward / dz
   int32_t V_local = 0, vocab_start = 0, V_true = 0;
-  int32_t n_tt = 0;                // token tiles
+  int32_t n_pm = 0;                // fwd / dz: 256-token pair tiles
   int32_t leaf0 = 0, n_leaves = 0; // fwd: global index of the shard's first leaf, leaf count
   const int64_t* y = nullptr;
   float* ws_m = nullptr;           // fwd: [n_leaves][T]
@@ -56,17 +62,18 @@ struct GemmArgs {
   int64_t out_ld = 0;
   int32_t out_rows = 0, out_cols = 0;
   int32_t out_f32 = 0;
-  int32_t n_mt = 0, n_nt = 0;
+  int32_t n_mt = 0, n_nt = 0;      // dH / dW: 256-row pair tiles along M, 256-column tiles along N
 };
 
-// Launchers (one translation unit each), enqueue on `stream`, return the launch status.
+// Launchers (one translation unit each): enqueue one cluster launch (pairs of CTAs,
+// as many pairs as can be resident, at most one per work item) on `stream`.
 cudaError_t launch_gemm_fwd(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                            int grid, cudaStream_t stream);
+                            cudaStream_t stream);
 cudaError_t launch_gemm_dz(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                           int grid, cudaStream_t stream);
+                           cudaStream_t stream);
 cudaError_t launch_gemm_dh(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                           int grid, cudaStream_t stream);
+                           cudaStream_t stream);
 cudaError_t launch_gemm_dw(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                           int grid, cudaStream_t stream);
+                           cudaStream_t stream);
 
 }  // namespace rlk
