@@ -37,6 +37,31 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_BYTES = 129 * 1024 * 1024
 
 
+def fwd_traffic_per_launch():
+    """dram read + write bytes of one forward launch on the Qwen3-8B workload, from the
+    committed ncu summary, or None if the kernel sources changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic_fwd_qwen3_8b.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if "=" in line and line.startswith("    "):
+                k, v = line.strip().split("=", 1)
+                vals[k.strip()] = v.strip()
+    try:
+        h = hashlib.sha256()
+        for name in vals["sources"].split():
+            with open(os.path.join(ROOT, "deterministic_token_logprob_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != vals["sources_sha256"]:
+            return None
+        return int(vals["traffic_bytes_per_launch"])
+    except (KeyError, OSError, ValueError):
+        return None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -228,6 +253,27 @@ class Path:
             rlk.shard_sum_bf16(self.dH_parts, out=self.dH)
 
 
+def rank_workload(w: workloads.Workload, rank: int) -> workloads.Workload:
+    """Rank `rank`'s batch: its own seeded h, y, g (seed = rank); W (model state) is shared."""
+    return workloads.Workload(w.name, T=w.T, H=w.H, V=w.V, V_true=w.V_true, seed=rank,
+                              backward=w.backward, g_kind=w.g_kind, shards=w.shards)
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest x over all ranks (the job's elapsed time is its slowest rank's)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, steps: int, max_total_ms: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * world * steps / (max_total_ms / 1e3)
+
+
 def gpu_uuid(torch, device):
     try:
         return "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
@@ -250,8 +296,7 @@ def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int)
 
     # model weight shared by all ranks (seed 0); each rank its own batch
     W_bits = workloads.make_W(w.V, w.H, seed=0)
-    wr = workloads.Workload(w.name, T=w.T, H=w.H, V=w.V, V_true=w.V_true, seed=rank,
-                            g_kind=w.g_kind, shards=w.shards)
+    wr = rank_workload(w, rank)
     d = workloads.make_inputs(wr, with_W=False)
     d["W"] = W_bits
     path = Path(rlk, torch, wr, d, device)
@@ -288,12 +333,9 @@ def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int)
     total_ms = t_start.elapsed_time(t_end)
     fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
     bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, device)
     ms_per_step = total_ms / K
-    tokens_per_s = w.T * world * K / (total_ms / 1e3)
+    tokens_per_s = job_tokens_per_s(w.T, world, K, total_ms)
 
     flops_fwd = 2.0 * w.T * w.H * w.V_true
     fwd_avg = statistics.mean(fwd_ms)
@@ -310,7 +352,8 @@ def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int)
         "gpu_launches": K * path.launches_per_step(),
         "roofline": {"bound": "tensor", "kernel": "forward tile GEMM + online statistics",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": fwd_traffic_per_launch() if w.name == "qwen3_8b" else None,
                      "peak_source": f"{peaks_src} bf16 burst",
                      "algorithmic_flops_per_launch": flops_fwd, "avg_launch_ms": fwd_avg},
         "step_roofline": {"flops_counted": step_flops, "roofline_ms": roofline_ms,
@@ -322,12 +365,45 @@ def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int)
 
     if rank == 0 and world == 1 and not args.quick:
         line["fwd_only"] = fwd_only(rlk, torch, W_bits, path, device, args, peak)
+        if not w.shards:
+            line["saved_logits"] = saved_logits_leg(rlk, torch, path, wr, device, args, peak, peak_sus)
         line["e2e"] = e2e(rlk, torch, path, wr, d, device, args)
         rate, cores, sample = oracle_sample_rate(wr, d)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def saved_logits_leg(rlk, torch, path, w, device, args, peak, peak_sus):
+    """The same fwd+bwd step through the saved-logits pair (forward stores fp32 z,
+    backward forms dz from it instead of recomputing the logits GEMM)."""
+    z = rlk.saved_logits_buffer(w.T, w.V, device)
+
+    def step():
+        rlk.linear_logp_fwd_save(path.h, path.W, path.y, w.V_true, z_saved=z,
+                                 out=(path.logp, path.lse), workspace=path.fws)
+        rlk.linear_logp_bwd_saved(path.h, path.W, path.y, path.lse, path.g, z, w.V_true,
+                                  out=(path.dH, path.dW), workspace=path.bws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(device)
+    K = args.steps
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(K):
+        step()
+    b.record()
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / K
+    del z
+    step_flops = 3.0 * 2.0 * w.T * w.H * w.V_true
+    return {"tokens_per_s": w.T / (ms / 1e3), "ms_per_step": ms,
+            "frac_of_burst": step_flops / (peak * 1e12) / (ms / 1e3),
+            "frac_of_sustained": step_flops / (peak_sus * 1e12) / (ms / 1e3),
+            "saved_logits_bytes": rlk.saved_logits_bytes(w.T, w.V), "steps": K,
+            "gpu_launches_per_step": 5}
 
 
 def fwd_only(rlk, torch, W_bits, path, device, args, peak):

@@ -9,5 +9,6 @@ sum_t g_t logp_t. It is a C ABI shared library (include/rlk.h, built into
 from ._binding import (  # noqa: F401
     LEAF_WIDTH, MAX_SHARDS, RLK_ERR_CUDA, RLK_ERR_INVALID_ARG, RLK_ERR_UNSUPPORTED,
     RLK_ERR_WORKSPACE, RLK_FLAG_BAD_TARGET, RLK_FLAG_TIMEOUT, RLK_OK, RlkError,
-    bwd_workspace_bytes, fwd_workspace_bytes, lib, library_path, linear_logp_bwd, linear_logp_fwd,
-    lse_merge, shard_bounds, shard_sum_bf16, version)
+    bwd_workspace_bytes, fwd_workspace_bytes, lib, library_path, linear_logp_bwd,
+    linear_logp_bwd_saved, linear_logp_fwd, linear_logp_fwd_save, lse_merge, saved_logits_buffer,
+    saved_logits_bytes, shard_bounds, shard_sum_bf16, version)

@@ -65,6 +65,14 @@ def _load():
         lib.rlk_linear_logp_bwd.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, P, I32, P, P,
                                             P, SZ, P]
         lib.rlk_linear_logp_bwd.restype = ctypes.c_int
+        lib.rlk_saved_logits_bytes.argtypes = [I64, I64]
+        lib.rlk_saved_logits_bytes.restype = SZ
+        lib.rlk_linear_logp_fwd_save.argtypes = [P, P, P, I64, I64, I64, I64, I64, P, P, P, P, SZ,
+                                                 P, P, SZ, P]
+        lib.rlk_linear_logp_fwd_save.restype = ctypes.c_int
+        lib.rlk_linear_logp_bwd_saved.argtypes = [P, P, P, P, P, P, SZ, I64, I64, I64, I64, I64, P,
+                                                  I32, P, P, P, SZ, P]
+        lib.rlk_linear_logp_bwd_saved.restype = ctypes.c_int
         lib.rlk_shard_sum_bf16.argtypes = [P, I32, I64, P, P]
         lib.rlk_shard_sum_bf16.restype = ctypes.c_int
         lib.rlk_status_string.argtypes = [ctypes.c_int]
@@ -227,6 +235,94 @@ def linear_logp_bwd(h: torch.Tensor, W: torch.Tensor, y: torch.Tensor, lse: torc
                                      1 if dH_fp32_partial else 0, _ptr(dW), _ptr(err_flag),
                                      _ptr(ws), nbytes, _stream_handle(stream))
     _check("rlk_linear_logp_bwd", st)
+    return dH, dW
+
+
+def saved_logits_bytes(T: int, V_local: int) -> int:
+    return int(_load().rlk_saved_logits_bytes(T, V_local))
+
+
+def saved_logits_buffer(T: int, V_local: int, device="cuda") -> torch.Tensor:
+    """An fp32 [T, round_up(V_local, 256)] buffer for the saved-logits pair."""
+    return torch.empty((T, -(-V_local // 256) * 256), dtype=torch.float32, device=device)
+
+
+def linear_logp_fwd_save(h: torch.Tensor, W: torch.Tensor, y: torch.Tensor, V_true: int, *,
+                         vocab_start: int = 0, partial: bool = False,
+                         z_saved: Optional[torch.Tensor] = None,
+                         out: Optional[Sequence[torch.Tensor]] = None,
+                         err_flag: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None, stream=None):
+    """rlk_linear_logp_fwd_save: the forward that also stores its fp32 logits.
+
+    Returns ((logp, lse) or partial, z_saved).
+    """
+    _need(h, "h", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 2)
+    _need(y, "y", torch.int64, 1)
+    T, H = h.shape
+    V_local = W.shape[0]
+    if W.shape[1] != H or y.shape[0] != T:
+        raise ValueError("shape mismatch")
+    dev = h.device
+    if z_saved is None:
+        z_saved = saved_logits_buffer(T, V_local, dev)
+    _need(z_saved, "z_saved", torch.float32, 2)
+    ws = _workspace(fwd_workspace_bytes(T, H, V_local), dev, workspace)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    if partial:
+        p = out[0] if out is not None else torch.empty((T, 3), dtype=torch.float32, device=dev)
+        _need(p, "partial", torch.float32, 2)
+        logp = lse = None
+    else:
+        p = None
+        if out is not None:
+            logp, lse = out
+        else:
+            logp = torch.empty(T, dtype=torch.float32, device=dev)
+            lse = torch.empty(T, dtype=torch.float32, device=dev)
+    if err_flag is not None:
+        _need(err_flag, "err_flag", torch.int32, 1)
+    st = _load().rlk_linear_logp_fwd_save(
+        _ptr(h), _ptr(W), _ptr(y), T, H, V_local, int(vocab_start), int(V_true), _ptr(logp),
+        _ptr(lse), _ptr(p), _ptr(z_saved), z_saved.numel() * 4, _ptr(err_flag), _ptr(ws), nbytes,
+        _stream_handle(stream))
+    _check("rlk_linear_logp_fwd_save", st)
+    return (p if partial else (logp, lse)), z_saved
+
+
+def linear_logp_bwd_saved(h: torch.Tensor, W: torch.Tensor, y: torch.Tensor, lse: torch.Tensor,
+                          g: torch.Tensor, z_saved: torch.Tensor, V_true: int, *,
+                          vocab_start: int = 0, dH_fp32_partial: bool = False,
+                          want_dH: bool = True, want_dW: bool = True,
+                          out: Optional[Tuple[Optional[torch.Tensor], Optional[torch.Tensor]]] = None,
+                          err_flag: Optional[torch.Tensor] = None,
+                          workspace: Optional[torch.Tensor] = None, stream=None):
+    """rlk_linear_logp_bwd_saved: the backward from the forward's saved logits -> (dH, dW)."""
+    _need(h, "h", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 2)
+    _need(y, "y", torch.int64, 1)
+    _need(lse, "lse", torch.float32, 1)
+    _need(g, "g", torch.float32, 1)
+    _need(z_saved, "z_saved", torch.float32, 2)
+    T, H = h.shape
+    V_local = W.shape[0]
+    dev = h.device
+    if out is not None:
+        dH, dW = out
+    else:
+        dH = (torch.empty((T, H), dtype=torch.float32 if dH_fp32_partial else torch.bfloat16,
+                          device=dev) if want_dH else None)
+        dW = torch.empty((V_local, H), dtype=torch.float32, device=dev) if want_dW else None
+    if err_flag is not None:
+        _need(err_flag, "err_flag", torch.int32, 1)
+    ws = _workspace(bwd_workspace_bytes(T, H, V_local), dev, workspace)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    st = _load().rlk_linear_logp_bwd_saved(
+        _ptr(h), _ptr(W), _ptr(y), _ptr(lse), _ptr(g), _ptr(z_saved), z_saved.numel() * 4, T, H,
+        V_local, int(vocab_start), int(V_true), _ptr(dH), 1 if dH_fp32_partial else 0, _ptr(dW),
+        _ptr(err_flag), _ptr(ws), nbytes, _stream_handle(stream))
+    _check("rlk_linear_logp_bwd_saved", st)
     return dH, dW
 
 

@@ -164,6 +164,46 @@ __global__ void shard_sum_kernel(const float* p, int S, int64_t n, uint16_t* out
   }
 }
 
+// dz from saved fp32 logits: eight consecutive columns of one row per thread.
+// Same arithmetic as the recompute epilogue (dz_target / dz_other), so the two
+// backward paths produce identical bits.
+__global__ void dz_from_logits_kernel(const float* z, int64_t z_ld, const int64_t* y,
+                                      const float* lse, const float* g, int T, int Vd,
+                                      int V_valid, int vocab_start, int V_true, uint16_t* dz,
+                                      int64_t dz_ld, int32_t* err_flag) {
+  const int64_t groups = static_cast<int64_t>(Vd / 8);
+  const int64_t total = static_cast<int64_t>(T) * groups;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(idx / groups);
+    const int c0 = static_cast<int>(idx - static_cast<int64_t>(t) * groups) * 8;
+    const int64_t yt = y[t];
+    const bool yvalid = yt >= 0 && yt < V_true;
+    if (!yvalid && c0 == 0 && err_flag) atomicOr(err_flag, RLK_FLAG_BAD_TARGET);
+    float d[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d[i] = 0.f;
+    if (yvalid && c0 < V_valid) {
+      const float4* zp = reinterpret_cast<const float4*>(z + static_cast<size_t>(t) * z_ld + c0);
+      const float4 z0 = zp[0], z1 = zp[1];
+      const float zv[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+      const float gt = g[t];
+      const float nl = neg_scaled(lse[t]);
+      const float ng = -gt;
+      const int64_t tl = yt - vocab_start - c0;  // target column inside this group, if any
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (c0 + i < V_valid) d[i] = (i == tl) ? dz_target(zv[i], nl, gt) : dz_other(zv[i], nl, ng);
+    }
+    uint4 w;
+    w.x = pack_bf16x2(d[0], d[1]);
+    w.y = pack_bf16x2(d[2], d[3]);
+    w.z = pack_bf16x2(d[4], d[5]);
+    w.w = pack_bf16x2(d[6], d[7]);
+    *reinterpret_cast<uint4*>(dz + static_cast<size_t>(t) * dz_ld + c0) = w;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // host helpers
 // ---------------------------------------------------------------------------
@@ -257,6 +297,11 @@ size_t fwd_ws_array_bytes(int64_t T, int64_t V_local) {
   return static_cast<size_t>(round_up(ceil_div(V_local, LEAF) * T * 4, 256));
 }
 
+size_t saved_logits_bytes(int64_t T, int64_t V_local) {
+  if (T <= 0 || V_local <= 0) return 0;
+  return static_cast<size_t>(T) * static_cast<size_t>(round_up(V_local, BN)) * 4;
+}
+
 }  // namespace
 }  // namespace rlk
 
@@ -283,11 +328,16 @@ size_t rlk_linear_logp_fwd_workspace(int64_t T, int64_t H, int64_t V_local) {
   return 3 * fwd_ws_array_bytes(T, V_local);
 }
 
-rlk_status rlk_linear_logp_fwd(const void* h, const void* W, const int64_t* y, int64_t T,
-                               int64_t H, int64_t V_local, int64_t vocab_start, int64_t V_true,
-                               float* logp, float* lse, rlk_lse_partial* partial,
-                               int32_t* err_flag, void* workspace, size_t workspace_bytes,
-                               void* stream) {
+}  // extern "C"
+
+namespace rlk {
+namespace {
+
+// The forward; z_saved (optional) receives the fp32 logits of the shard's columns.
+rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, int64_t H,
+                    int64_t V_local, int64_t vocab_start, int64_t V_true, float* logp, float* lse,
+                    rlk_lse_partial* partial, float* z_saved, size_t z_saved_bytes,
+                    int32_t* err_flag, void* workspace, size_t workspace_bytes, void* stream) {
   rlk_status st = common_checks(h, W, y, T, H, V_local, vocab_start, V_true);
   if (st != RLK_OK) return st;
   if (T > 0 && !partial && !logp && !lse) return RLK_ERR_INVALID_ARG;
@@ -295,6 +345,8 @@ rlk_status rlk_linear_logp_fwd(const void* h, const void* W, const int64_t* y, i
   st = shard_geometry(V_local, vocab_start, V_true, &g);
   if (st != RLK_OK) return st;
   if (!partial && (vocab_start != 0 || !g.reaches_end)) return RLK_ERR_INVALID_ARG;
+  if (z_saved && (!aligned16(z_saved) || z_saved_bytes < saved_logits_bytes(T, V_local)))
+    return RLK_ERR_INVALID_ARG;
   if (T == 0) return RLK_OK;
   const size_t arr = fwd_ws_array_bytes(T, V_local);
   if (g.n_leaves_local > 0) {
@@ -325,6 +377,8 @@ rlk_status rlk_linear_logp_fwd(const void* h, const void* W, const int64_t* y, i
     a.ws_m = ws_m;
     a.ws_s = ws_s;
     a.ws_zt = ws_zt;
+    a.z_out = z_saved;
+    a.z_ld = round_up(V_local, BN);
     a.err_flag = err_flag;
     if (launch_gemm_fwd(tmA, tmB, a, s) != cudaSuccess) return RLK_ERR_CUDA;
   }
@@ -352,6 +406,33 @@ rlk_status rlk_linear_logp_fwd(const void* h, const void* W, const int64_t* y, i
   return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
 }
 
+}  // namespace
+}  // namespace rlk
+
+extern "C" {
+
+rlk_status rlk_linear_logp_fwd(const void* h, const void* W, const int64_t* y, int64_t T,
+                               int64_t H, int64_t V_local, int64_t vocab_start, int64_t V_true,
+                               float* logp, float* lse, rlk_lse_partial* partial,
+                               int32_t* err_flag, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  return fwd_impl(h, W, y, T, H, V_local, vocab_start, V_true, logp, lse, partial, nullptr, 0,
+                  err_flag, workspace, workspace_bytes, stream);
+}
+
+size_t rlk_saved_logits_bytes(int64_t T, int64_t V_local) { return saved_logits_bytes(T, V_local); }
+
+rlk_status rlk_linear_logp_fwd_save(const void* h, const void* W, const int64_t* y, int64_t T,
+                                    int64_t H, int64_t V_local, int64_t vocab_start,
+                                    int64_t V_true, float* logp, float* lse,
+                                    rlk_lse_partial* partial, float* z_saved,
+                                    size_t z_saved_bytes, int32_t* err_flag, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  if (T > 0 && !z_saved) return RLK_ERR_INVALID_ARG;
+  return fwd_impl(h, W, y, T, H, V_local, vocab_start, V_true, logp, lse, partial, z_saved,
+                  z_saved_bytes, err_flag, workspace, workspace_bytes, stream);
+}
+
 rlk_status rlk_lse_merge(const rlk_lse_partial* partials, int32_t S, int64_t T, float* logp,
                          float* lse, void* stream) {
   if (T < 0 || (T > 0 && (!partials || !logp || !lse))) return RLK_ERR_INVALID_ARG;
@@ -370,11 +451,18 @@ size_t rlk_linear_logp_bwd_workspace(int64_t T, int64_t H, int64_t V_local) {
   return static_cast<size_t>(T) * static_cast<size_t>(round_up(V_local, BN)) * 2;
 }
 
-rlk_status rlk_linear_logp_bwd(const void* h, const void* W, const int64_t* y, const float* lse,
-                               const float* g, int64_t T, int64_t H, int64_t V_local,
-                               int64_t vocab_start, int64_t V_true, void* dH,
-                               int32_t dH_fp32_partial, float* dW, int32_t* err_flag,
-                               void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace rlk {
+namespace {
+
+// The backward; with z_saved the dz tiles come from the saved logits instead of
+// a recomputed GEMM.
+rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float* lse,
+                    const float* g, const float* z_saved, int64_t T, int64_t H, int64_t V_local,
+                    int64_t vocab_start, int64_t V_true, void* dH, int32_t dH_fp32_partial,
+                    float* dW, int32_t* err_flag, void* workspace, size_t workspace_bytes,
+                    void* stream) {
   rlk_status st = common_checks(h, W, y, T, H, V_local, vocab_start, V_true);
   if (st != RLK_OK) return st;
   if (T > 0 && (!lse || !g)) return RLK_ERR_INVALID_ARG;
@@ -388,8 +476,18 @@ rlk_status rlk_linear_logp_bwd(const void* h, const void* W, const int64_t* y, c
   uint16_t* dz = static_cast<uint16_t*>(workspace);
   const int32_t n_pm = static_cast<int32_t>(ceil_div(T, PAIR_M));
 
-  // 1. recompute z tiles -> dz (bf16) workspace
-  {
+  // 1. dz (bf16) workspace: from the saved logits, or from recomputed z tiles
+  if (z_saved) {
+    const int64_t V_valid = std::max<int64_t>(0, std::min<int64_t>(V_true - vocab_start, V_local));
+    const int64_t total = T * (Vd / 8);
+    const int threads = 256;
+    const int64_t blocks = std::min<int64_t>(ceil_div(total, threads), 1 << 20);
+    dz_from_logits_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(
+        z_saved, Vd, y, lse, g, static_cast<int>(T), static_cast<int>(Vd),
+        static_cast<int>(V_valid), static_cast<int>(vocab_start), static_cast<int>(V_true), dz, Vd,
+        err_flag);
+    if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
+  } else {
     CUtensorMap tmA, tmB;
     if (!encode_2d(&tmA, h, H, T, H, 64, BM)) return RLK_ERR_CUDA;
     if (!encode_2d(&tmB, W, H, V_local, H, 64, B_HALF)) return RLK_ERR_CUDA;
@@ -459,6 +557,32 @@ rlk_status rlk_linear_logp_bwd(const void* h, const void* W, const int64_t* y, c
     if (launch_gemm_dw(tmA, tmB, a, s) != cudaSuccess) return RLK_ERR_CUDA;
   }
   return RLK_OK;
+}
+
+}  // namespace
+}  // namespace rlk
+
+extern "C" {
+
+rlk_status rlk_linear_logp_bwd(const void* h, const void* W, const int64_t* y, const float* lse,
+                               const float* g, int64_t T, int64_t H, int64_t V_local,
+                               int64_t vocab_start, int64_t V_true, void* dH,
+                               int32_t dH_fp32_partial, float* dW, int32_t* err_flag,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(h, W, y, lse, g, nullptr, T, H, V_local, vocab_start, V_true, dH,
+                  dH_fp32_partial, dW, err_flag, workspace, workspace_bytes, stream);
+}
+
+rlk_status rlk_linear_logp_bwd_saved(const void* h, const void* W, const int64_t* y,
+                                     const float* lse, const float* g, const float* z_saved,
+                                     size_t z_saved_bytes, int64_t T, int64_t H, int64_t V_local,
+                                     int64_t vocab_start, int64_t V_true, void* dH,
+                                     int32_t dH_fp32_partial, float* dW, int32_t* err_flag,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (T > 0 && (!z_saved || !aligned16(z_saved) || z_saved_bytes < saved_logits_bytes(T, V_local)))
+    return RLK_ERR_INVALID_ARG;
+  return bwd_impl(h, W, y, lse, g, z_saved, T, H, V_local, vocab_start, V_true, dH,
+                  dH_fp32_partial, dW, err_flag, workspace, workspace_bytes, stream);
 }
 
 rlk_status rlk_shard_sum_bf16(const float* partials, int32_t S, int64_t n, void* out, void* stream) {

@@ -113,11 +113,14 @@ template <int MODE>
 __device__ void producer_loop(const CUtensorMap* tmA, const CUtensorMap* tmB, const GemmArgs& a,
                               uint8_t* smem, uint64_t* full, uint64_t* empty, const PairCtx& c) {
   // L2 policy per operand: h is re-read by every leaf / vocab tile (fwd, dz) or by
-  // every vocab tile of dW, so it is kept; everything else is normal.
+  // every vocab tile of dW, so it is kept; the W tiles of fwd / dz are used by all
+  // token tiles within a short window and then never again, so they go first.
   const uint64_t pol_keep = policy_evict_last();
   const uint64_t pol_norm = policy_evict_normal();
-  const uint64_t polA = (MODE == MODE_FWD || MODE == MODE_DZ) ? pol_keep : pol_norm;
-  const uint64_t polB = (MODE == MODE_DW) ? pol_keep : pol_norm;
+  const uint64_t pol_first = policy_evict_first();
+  constexpr bool kZ = (MODE == MODE_FWD || MODE == MODE_DZ);
+  const uint64_t polA = kZ ? pol_keep : pol_norm;
+  const uint64_t polB = (MODE == MODE_DW) ? pol_keep : (kZ ? pol_first : pol_norm);
   const uint32_t r = c.rank;
   uint32_t issued = 0;
   bool ok = true;
@@ -340,10 +343,20 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
         const int c0 = n0 + a.vocab_start + j * BN;  // global column of the tile's first column
         const int vcols = min(BN, a.V_true - c0);
         const int tl = (yt >= c0 && yt < static_cast<int64_t>(c0) + vcols) ? static_cast<int>(yt - c0) : -1;
+        float* zrow = (a.z_out && t < a.T)
+                          ? a.z_out + static_cast<size_t>(t) * a.z_ld + (n0 + j * BN) : nullptr;
 #pragma unroll 1
         for (int ch = 0; ch < BN; ch += 64) {
           float v[64];
           tmem_ld64(taddr + ch, v);
+          if (zrow) {  // saved logits: the accumulator exactly as computed
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              st_global_v4_hint(zrow + ch + 4 * q,
+                                make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
+                                           __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3])),
+                                pol_out);
+          }
           fwd_chunk(v, vcols - ch, tl - ch, st);
         }
       } else if constexpr (MODE == MODE_DZ) {
@@ -363,10 +376,10 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
           if (any_target) {
 #pragma unroll
             for (int i = 0; i < 64; ++i)
-              if (i == tli) d_target = __fmul_rn(g_t, __fsub_rn(1.f, exp_shifted(v[i], nl)));
+              if (i == tli) d_target = dz_target(v[i], nl, g_t);
           }
 #pragma unroll
-          for (int i = 0; i < 64; ++i) v[i] = __fmul_rn(ng, exp_shifted(v[i], nl));
+          for (int i = 0; i < 64; ++i) v[i] = dz_other(v[i], nl, ng);
           if (any_target) {
 #pragma unroll
             for (int i = 0; i < 64; ++i)

@@ -53,6 +53,8 @@ struct GemmArgs {
   float* ws_m = nullptr;           // fwd: [n_leaves][T]
   float* ws_s = nullptr;
   float* ws_zt = nullptr;
+  float* z_out = nullptr;          // fwd, optional: fp32 logits [T][z_ld] (local columns)
+  int64_t z_ld = 0;
   const float* lse = nullptr;      // dz
   const float* g = nullptr;
   uint16_t* dz = nullptr;          // dz: bf16 bits [T][dz_ld]

@@ -327,6 +327,17 @@ __device__ __forceinline__ float exp_shifted(float x, float nb) {
   return ex2_approx(__fmaf_rn(x, kLog2e, nb));
 }
 
+// dz of one logit z of a row with upstream gradient g and nl = neg_scaled(lse):
+// g (1 - e(z - lse)) at the target column, -g e(z - lse) elsewhere. Used by the
+// recompute epilogue and by the saved-logits kernel, so both give the same bits.
+__device__ __forceinline__ float dz_target(float z, float nl, float g) {
+  return __fmul_rn(g, __fsub_rn(1.f, exp_shifted(z, nl)));
+}
+
+__device__ __forceinline__ float dz_other(float z, float nl, float neg_g) {
+  return __fmul_rn(neg_g, exp_shifted(z, nl));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

@@ -184,6 +184,38 @@ RLK_API rlk_status rlk_linear_logp_bwd(const void* h, const void* W, const int64
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Saved-logits variant of the pair above: the forward also stores the fp32
+ * logits it computed and the backward forms dz from them instead of recomputing
+ * the logits GEMM (the "save-logits fused-tile full-gradient path" named in
+ * "Announcing RL-Kernel for vime", section "Validation and Benchmarks"). The
+ * saved logits are the accumulator values bit for bit and dz uses the same
+ * arithmetic, so logp, lse, dH and dW are bit-identical to the recompute path;
+ * the price is rlk_saved_logits_bytes of device memory between the two calls.
+ *
+ *   z_saved  device fp32 [T][round_up(V_local, 256)], 16-byte aligned, caller-owned;
+ *            written by rlk_linear_logp_fwd_save for the shard's columns below
+ *            V_true, read by rlk_linear_logp_bwd_saved; z_saved_bytes must be at
+ *            least rlk_saved_logits_bytes(T, V_local) (else RLK_ERR_INVALID_ARG)
+ * Every other argument is as in rlk_linear_logp_fwd / rlk_linear_logp_bwd.
+ */
+RLK_API size_t rlk_saved_logits_bytes(int64_t T, int64_t V_local);
+
+RLK_API rlk_status rlk_linear_logp_fwd_save(const void* h, const void* W, const int64_t* y,
+                                            int64_t T, int64_t H, int64_t V_local,
+                                            int64_t vocab_start, int64_t V_true, float* logp,
+                                            float* lse, rlk_lse_partial* partial, float* z_saved,
+                                            size_t z_saved_bytes, int32_t* err_flag,
+                                            void* workspace, size_t workspace_bytes, void* stream);
+
+RLK_API rlk_status rlk_linear_logp_bwd_saved(const void* h, const void* W, const int64_t* y,
+                                             const float* lse, const float* g,
+                                             const float* z_saved, size_t z_saved_bytes, int64_t T,
+                                             int64_t H, int64_t V_local, int64_t vocab_start,
+                                             int64_t V_true, void* dH, int32_t dH_fp32_partial,
+                                             float* dW, int32_t* err_flag, void* workspace,
+                                             size_t workspace_bytes, void* stream);
+
+/*
  * out[i] = bf16(((p[0][i] + p[1][i]) + p[2][i]) + ...), the fixed ascending-order
  * sum of S fp32 partials laid out [S][n], rounded once to bf16 (RNE). Used to
  * combine per-shard dH partials. partials, out: device, 16-byte aligned.

@@ -19,7 +19,7 @@ def lib():
     from deterministic_token_logprob_gb300 import build
     build.build()
     import deterministic_token_logprob_gb300 as rlk
-    return rlk.lib()
+    return rlk.lib()   # the binding declares argtypes / restype of every entry point
 
 
 def declared_functions():
@@ -145,3 +145,19 @@ def test_merge_and_sum_argument_errors(lib):
     assert lib.rlk_shard_sum_bf16(FAKE, 2, 0, FAKE, None) == OK
     assert lib.rlk_shard_sum_bf16(MISALIGNED, 2, 8, FAKE, None) == INVALID
     assert lib.rlk_shard_sum_bf16(FAKE, 0, 8, FAKE, None) == INVALID
+
+
+def test_saved_logits_queries_and_errors(lib):
+    assert lib.rlk_saved_logits_bytes(8192, 151936) == 8192 * 152064 * 4
+    assert lib.rlk_saved_logits_bytes(0, 151936) == 0
+    need = lib.rlk_saved_logits_bytes(4, 4096)
+    args = (FAKE, FAKE, FAKE, 4, 64, 4096, 0, 4096, FAKE, FAKE, None)
+    assert lib.rlk_linear_logp_fwd_save(*args, None, need, None, FAKE, 1 << 30, None) == INVALID
+    assert lib.rlk_linear_logp_fwd_save(*args, FAKE, need - 1, None, FAKE, 1 << 30, None) == INVALID
+    assert lib.rlk_linear_logp_fwd_save(*args, MISALIGNED, need, None, FAKE, 1 << 30, None) == INVALID
+    bargs = (FAKE, FAKE, FAKE, FAKE, FAKE)
+    rest = (4, 64, 4096, 0, 4096, FAKE, 0, FAKE, None, FAKE, 1 << 30, None)
+    assert lib.rlk_linear_logp_bwd_saved(*bargs, None, need, *rest) == INVALID
+    assert lib.rlk_linear_logp_bwd_saved(*bargs, FAKE, need - 1, *rest) == INVALID
+    zero = (0, 64, 4096, 0, 4096, None, 0, None, None, None, 0, None)
+    assert lib.rlk_linear_logp_bwd_saved(None, FAKE, None, None, None, None, 0, *zero) == OK

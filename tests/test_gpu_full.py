@@ -158,3 +158,19 @@ def test_batch_invariance_full(rlk, oracle_mod, W8b):
     bits, W = W8b
     w = workloads.QWEN3_8B
     _invariance(rlk, w.H, w.V, w.V_true, bits, W, workloads.INVARIANCE_T, oracle_mod)
+
+
+def test_qwen3_8b_saved_logits_bitwise(rlk, W8b):
+    """The saved-logits pair reproduces the recompute path bit for bit at full size."""
+    w = workloads.QWEN3_8B
+    _, W = W8b
+    d = workloads.make_inputs(w, with_W=False)
+    h, y, g = dev_bf16(d["h"]), dev(d["y"]), dev(d["g"])
+    logp, lse = rlk.linear_logp_fwd(h, W, y, w.V_true)
+    dH, dW = rlk.linear_logp_bwd(h, W, y, lse, g, w.V_true)
+    (logp2, lse2), z = rlk.linear_logp_fwd_save(h, W, y, w.V_true)
+    assert torch.equal(logp, logp2) and torch.equal(lse, lse2)
+    del logp2, lse2
+    dH2, dW2 = rlk.linear_logp_bwd_saved(h, W, y, lse, g, z, w.V_true)
+    assert torch.equal(dH, dH2)
+    assert torch.equal(dW, dW2)

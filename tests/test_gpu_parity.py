@@ -198,3 +198,38 @@ def test_shard_sum_bf16(rlk):
         out = rlk.shard_sum_bf16(p)
         ref = ((p[0] + p[1]) + p[2]).to(torch.bfloat16)
         assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("T,H,V,Vt", [(300, 512, 20480, 20000), (129, 200, 2500, 2345), (1, 64, 256, 256)])
+def test_saved_logits_path_is_bitwise_the_recompute_path(rlk, T, H, V, Vt):
+    d = _inputs(T, H, V, Vt, seed=T * 7 + 1)
+    h, W, y, g = dev_bf16(d["h"]), dev_bf16(d["W"]), dev(d["y"]), dev(d["g"])
+    logp, lse = rlk.linear_logp_fwd(h, W, y, Vt)
+    (logp2, lse2), z = rlk.linear_logp_fwd_save(h, W, y, Vt)
+    assert torch.equal(logp, logp2) and torch.equal(lse, lse2)
+    dH, dW = rlk.linear_logp_bwd(h, W, y, lse, g, Vt)
+    dH2, dW2 = rlk.linear_logp_bwd_saved(h, W, y, lse, g, z, Vt)
+    assert torch.equal(dH, dH2) and torch.equal(dW, dW2)
+    # the saved logits are the fp32 products h W^T of the valid columns
+    ref = host_bf16_to_f64(h) @ host_bf16_to_f64(W).T
+    got = z[:, :Vt].cpu().numpy().astype(np.float64)
+    np.testing.assert_allclose(got, ref[:, :Vt], rtol=0, atol=1e-4 * max(1.0, np.abs(ref).max()))
+
+
+def test_saved_logits_sharded_and_invalid_targets(rlk):
+    T, H, V, Vt = 300, 512, 20480, 20000
+    d = _inputs(T, H, V, Vt, seed=77)
+    yb = d["y"].copy()
+    yb[[5, 200]] = [-3, Vt + 1]
+    h, W, y, g = dev_bf16(d["h"]), dev_bf16(d["W"]), dev(yb), dev(d["g"])
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    logp, lse = rlk.linear_logp_fwd(h, W, y, Vt)
+    dH, dW = rlk.linear_logp_bwd(h, W, y, lse, g, Vt)
+    for a, n in rlk.shard_bounds(V, Vt, 2):
+        _, z = rlk.linear_logp_fwd_save(h, W[a:a + n], y, Vt, vocab_start=a, partial=True)
+        dHp, dWp = rlk.linear_logp_bwd_saved(h, W[a:a + n], y, lse, g, z, Vt, vocab_start=a,
+                                             dH_fp32_partial=True, err_flag=err)
+        assert torch.equal(dWp, dW[a:a + n])
+        assert torch.all(dHp[[5, 200]] == 0)
+    torch.cuda.synchronize()
+    assert int(err.item()) & rlk.RLK_FLAG_BAD_TARGET
