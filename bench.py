@@ -367,6 +367,7 @@ def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int)
         line["fwd_only"] = fwd_only(rlk, torch, W_bits, path, device, args, peak)
         if not w.shards:
             line["saved_logits"] = saved_logits_leg(rlk, torch, path, wr, device, args, peak, peak_sus)
+            line["small_T_forward"] = small_t_leg(rlk, torch, path, device, peaks)
         line["e2e"] = e2e(rlk, torch, path, wr, d, device, args)
         rate, cores, sample = oracle_sample_rate(wr, d)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
@@ -404,6 +405,39 @@ def saved_logits_leg(rlk, torch, path, w, device, args, peak, peak_sus):
             "frac_of_sustained": step_flops / (peak_sus * 1e12) / (ms / 1e3),
             "saved_logits_bytes": rlk.saved_logits_bytes(w.T, w.V), "steps": K,
             "gpu_launches_per_step": 5}
+
+
+def small_t_leg(rlk, torch, path, device, peaks):
+    """Forward latency at small T (the batch-invariance workload's batch sizes) on the
+    Qwen3-8B weight: these calls stream W once and are HBM-bound; reported as achieved
+    GB/s of algorithmic bytes (W + h read, statistics written) against measured HBM."""
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    W = path.W
+    V, H = W.shape
+    Vt = path.w.V_true
+    out = {}
+    for T in (1, 7, 128, 1000):
+        h = torch.from_numpy(workloads.make_h(T, H, 9).view(np.int16)).view(torch.bfloat16).to(device)
+        y = torch.from_numpy(workloads.make_y(T, Vt, 9)).to(device)
+        logp = torch.empty(T, dtype=torch.float32, device=device)
+        lse = torch.empty(T, dtype=torch.float32, device=device)
+        ws = torch.empty(rlk.fwd_workspace_bytes(T, H, V), dtype=torch.uint8, device=device)
+        for _ in range(5):
+            rlk.linear_logp_fwd(h, W, y, Vt, out=(logp, lse), workspace=ws)
+        n = 20
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        a.record()
+        for _ in range(n):
+            rlk.linear_logp_fwd(h, W, y, Vt, out=(logp, lse), workspace=ws)
+        b.record()
+        torch.cuda.synchronize(device)
+        ms = a.elapsed_time(b) / n
+        nbytes = V * H * 2 + T * H * 2 + 3 * 4 * T * -(-V // 1024)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[str(T)] = {"us_per_call": ms * 1e3, "algorithmic_GBps": gbs, "frac_of_hbm": gbs / hbm}
+    out["note"] = "W and L2 are not flushed between calls; W (1.24 GB) exceeds L2 on its own"
+    return out
 
 
 def fwd_only(rlk, torch, W_bits, path, device, args, peak):

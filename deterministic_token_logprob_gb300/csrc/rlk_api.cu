@@ -84,24 +84,39 @@ struct TreeArgs {
 };
 
 // One thread per token: balanced pairwise merge of the shard's slots (a
-// binary-counter walk: after slot q, merge once per trailing one bit of q).
+// binary-counter walk: after slot q, merge once per trailing one bit of q). The
+// slot triples are fetched kPrefetch at a time ahead of the merges so that the
+// loads overlap instead of each waiting behind the previous merge.
+constexpr int kPrefetch = 16;
+
 __global__ void leaf_tree_kernel(const TreeArgs a) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= a.T) return;
   Triple stack[kMaxTreeDepth];
   int sp = 0;
-  for (int q = 0; q < a.slot_count; ++q) {
-    const int slot = a.slot_begin + q;
-    const int ss = slot / a.P, jj = slot - ss * a.P;
-    const int leaf = ss * a.L_ss + jj;
-    const int ll = leaf - a.leaf0;
-    Triple node = identity_triple();
-    if (jj < a.L_ss && leaf < a.n_leaves_global && ll >= 0 && ll < a.n_leaves_local) {
-      const size_t o = static_cast<size_t>(ll) * a.T + t;
-      node = Triple{a.ws_m[o], a.ws_s[o], a.ws_zt[o]};
+  for (int q0 = 0; q0 < a.slot_count; q0 += kPrefetch) {
+    Triple buf[kPrefetch];
+#pragma unroll
+    for (int i = 0; i < kPrefetch; ++i) {
+      const int slot = a.slot_begin + q0 + i;
+      const int ss = slot / a.P, jj = slot - ss * a.P;
+      const int leaf = ss * a.L_ss + jj;
+      const int ll = leaf - a.leaf0;
+      buf[i] = identity_triple();
+      if (q0 + i < a.slot_count && jj < a.L_ss && leaf < a.n_leaves_global && ll >= 0 &&
+          ll < a.n_leaves_local) {
+        const size_t o = static_cast<size_t>(ll) * a.T + t;
+        buf[i] = Triple{a.ws_m[o], a.ws_s[o], a.ws_zt[o]};
+      }
     }
-    for (int idx = q; idx & 1; idx >>= 1) node = merge_pair(stack[--sp], node);
-    stack[sp++] = node;
+#pragma unroll
+    for (int i = 0; i < kPrefetch; ++i) {
+      const int q = q0 + i;
+      if (q >= a.slot_count) break;
+      Triple node = buf[i];
+      for (int idx = q; idx & 1; idx >>= 1) node = merge_pair(stack[--sp], node);
+      stack[sp++] = node;
+    }
   }
   Triple r = stack[0];
   const int64_t y = a.y[t];
@@ -360,7 +375,7 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
 
   if (g.n_leaves_local > 0) {
     CUtensorMap tmA, tmB;
-    if (!encode_2d(&tmA, h, H, T, H, 64, BM)) return RLK_ERR_CUDA;
+    if (!encode_2d(&tmA, h, H, T, H, 64, 64)) return RLK_ERR_CUDA;  // 64-row boxes
     if (!encode_2d(&tmB, W, H, V_local, H, 64, B_HALF)) return RLK_ERR_CUDA;
     GemmArgs a;
     a.T = static_cast<int32_t>(T);
@@ -489,7 +504,7 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
     if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
   } else {
     CUtensorMap tmA, tmB;
-    if (!encode_2d(&tmA, h, H, T, H, 64, BM)) return RLK_ERR_CUDA;
+    if (!encode_2d(&tmA, h, H, T, H, 64, 64)) return RLK_ERR_CUDA;  // 64-row boxes
     if (!encode_2d(&tmB, W, H, V_local, H, 64, B_HALF)) return RLK_ERR_CUDA;
     GemmArgs a;
     a.T = static_cast<int32_t>(T);
@@ -517,7 +532,7 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
       if (cudaMemsetAsync(dH, 0, static_cast<size_t>(T) * H * elem, s) != cudaSuccess) return RLK_ERR_CUDA;
     } else {
       CUtensorMap tmA, tmB;
-      if (!encode_2d(&tmA, dz, Vd, T, Vd, 64, BM)) return RLK_ERR_CUDA;
+      if (!encode_2d(&tmA, dz, Vd, T, Vd, 64, 64)) return RLK_ERR_CUDA;  // 64-row boxes
       if (!encode_2d(&tmB, W, H, V_local, H, 64, 64)) return RLK_ERR_CUDA;
       GemmArgs a;
       a.T = static_cast<int32_t>(T);

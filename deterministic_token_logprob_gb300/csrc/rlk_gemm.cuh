@@ -109,6 +109,14 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
 // ---------------------------------------------------------------------------
 // warp 0: TMA producer (one thread per CTA)
 // ---------------------------------------------------------------------------
+constexpr int A_BOX_ROWS = 64;                    // K-major A boxes: 64 rows x 64 K
+constexpr int A_BOX_BYTES = A_BOX_ROWS * BK * 2;  // 8 KiB
+
+// 64-row A boxes needed for a CTA whose first A row leaves `rows_left` valid rows.
+__device__ __forceinline__ int a_boxes(int rows_left) {
+  return rows_left <= 0 ? 0 : min(BM / A_BOX_ROWS, (rows_left + A_BOX_ROWS - 1) / A_BOX_ROWS);
+}
+
 template <int MODE>
 __device__ void producer_loop(const CUtensorMap* tmA, const CUtensorMap* tmB, const GemmArgs& a,
                               uint8_t* smem, uint64_t* full, uint64_t* empty, const PairCtx& c) {
@@ -119,6 +127,7 @@ __device__ void producer_loop(const CUtensorMap* tmA, const CUtensorMap* tmB, co
   const uint64_t pol_norm = policy_evict_normal();
   const uint64_t pol_first = policy_evict_first();
   constexpr bool kZ = (MODE == MODE_FWD || MODE == MODE_DZ);
+  constexpr bool kAPerRow = (MODE != MODE_DW);  // A rows are tokens (independent outputs)
   const uint64_t polA = kZ ? pol_keep : pol_norm;
   const uint64_t polB = (MODE == MODE_DW) ? pol_keep : (kZ ? pol_first : pol_norm);
   const uint32_t r = c.rank;
@@ -131,6 +140,14 @@ __device__ void producer_loop(const CUtensorMap* tmA, const CUtensorMap* tmB, co
       tile_origin<MODE>(a, item, j, m0, n0);
       const int am = m0 + r * BM;      // this CTA's A rows
       const int bn = n0 + r * B_HALF;  // this CTA's B rows
+      // Token-row A operands (fwd, dz, dH) load in 64-row boxes and skip boxes that lie
+      // wholly at or beyond T: accumulator rows are independent dot products, rows past T
+      // are never stored, and the zero fill would otherwise cost as much load bandwidth
+      // as real data (small batches).
+      const int boxes_mine = kAPerRow ? a_boxes(a.T - am) : 0;
+      const int boxes_pair = kAPerRow ? a_boxes(a.T - m0) + a_boxes(a.T - m0 - BM) : 0;
+      const uint32_t tx = kAPerRow ? static_cast<uint32_t>(boxes_pair * A_BOX_BYTES + PAIR * B_STAGE_BYTES)
+                                   : static_cast<uint32_t>(PAIR * STAGE_BYTES);
       for (int kb = 0; kb < a.n_kb; ++kb) {
         const uint32_t s = issued % STAGES, ph = (issued / STAGES) & 1u;
         if (!pair_wait(&empty[s], ph ^ 1u, c)) {
@@ -140,13 +157,15 @@ __device__ void producer_loop(const CUtensorMap* tmA, const CUtensorMap* tmB, co
         uint8_t* sA = smem + s * STAGE_BYTES;
         uint8_t* sB = sA + A_STAGE_BYTES;
         const uint32_t bar = map_to_cta(smem_u32(&full[s]), 0);  // the even CTA's barrier
-        if (r == 0) mbar_arrive_expect_tx(&full[s], PAIR * STAGE_BYTES);
+        if (r == 0) mbar_arrive_expect_tx(&full[s], tx);
         const int k0 = kb * BK;
+        if constexpr (kAPerRow) {
+          for (int q = 0; q < boxes_mine; ++q)            // h / dz, K-major boxes 64 x 64
+            tma_load_2d_pair(sA + q * A_BOX_BYTES, tmA, bar, k0, am + q * A_BOX_ROWS, polA);
+        }
         if constexpr (MODE == MODE_FWD || MODE == MODE_DZ) {
-          tma_load_2d_pair(sA, tmA, bar, k0, am, polA);   // h, K-major box 64 x 128
           tma_load_2d_pair(sB, tmB, bar, k0, bn, polB);   // W, K-major box 64 x 128
         } else if constexpr (MODE == MODE_DH) {
-          tma_load_2d_pair(sA, tmA, bar, k0, am, polA);   // dz, K-major box 64 x 128
 #pragma unroll
           for (int q = 0; q < B_HALF / 64; ++q)           // W[k0.., bn+64q..], MN-major 64 x 64
             tma_load_2d_pair(sB + q * MN_ATOM_BYTES, tmB, bar, bn + q * 64, k0, polB);
