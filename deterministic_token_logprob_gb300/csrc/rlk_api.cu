@@ -68,9 +68,7 @@ __device__ __noinline__ void finalize(Triple x, float* logp, float* lse) {
 constexpr int kMaxTreeDepth = 16;  // log2(max slots = 8 * 2048) + 1
 
 struct TreeArgs {
-  const float* ws_m;
-  const float* ws_s;
-  const float* ws_zt;  // [n_leaves_local][T]
+  const float* ws;     // [T][n_leaves_local][3]: (m, s, zt) of each (token, leaf)
   int32_t T;
   int32_t n_leaves_local, leaf0, n_leaves_global;
   int32_t L_ss, P;                // leaves per super-shard, slots per super-shard
@@ -83,42 +81,62 @@ struct TreeArgs {
   int32_t* err_flag;
 };
 
-// One thread per token: balanced pairwise merge of the shard's slots (a
-// binary-counter walk: after slot q, merge once per trailing one bit of q). The
-// slot triples are fetched kPrefetch at a time ahead of the merges so that the
-// loads overlap instead of each waiting behind the previous merge.
-constexpr int kPrefetch = 16;
+__device__ __forceinline__ Triple load_slot(const TreeArgs& a, int t, int q) {
+  const int slot = a.slot_begin + q;
+  const int ss = slot / a.P, jj = slot - ss * a.P;
+  const int leaf = ss * a.L_ss + jj;
+  const int ll = leaf - a.leaf0;
+  if (jj < a.L_ss && leaf < a.n_leaves_global && ll >= 0 && ll < a.n_leaves_local) {
+    const float* p = a.ws + (static_cast<size_t>(t) * a.n_leaves_local + ll) * 3;
+    return Triple{p[0], p[1], p[2]};
+  }
+  return identity_triple();
+}
+
+__device__ __forceinline__ Triple shfl_xor_triple(const Triple& x, int d) {
+  return Triple{__shfl_xor_sync(0xffffffffu, x.m, d), __shfl_xor_sync(0xffffffffu, x.s, d),
+                __shfl_xor_sync(0xffffffffu, x.zt, d)};
+}
+
+// One warp per token: the balanced pairwise tree over the shard's slot_count slots
+// (a power of two). Lane L merges its run of consecutive slots with a binary-counter
+// walk (after slot q, merge once per trailing one bit of q) -- the tree's lower
+// levels -- then the lanes combine pairwise by xor-shuffles, the lower lane's
+// subtree always the left operand: the same tree, node for node, as a sequential
+// walk over all slots.
 
 __global__ void leaf_tree_kernel(const TreeArgs a) {
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= a.T) return;
-  Triple stack[kMaxTreeDepth];
-  int sp = 0;
-  for (int q0 = 0; q0 < a.slot_count; q0 += kPrefetch) {
-    Triple buf[kPrefetch];
+  const int t = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= a.T) return;  // warp-uniform
+  const int per = a.slot_count >= 32 ? a.slot_count >> 5 : 1;
+  const int lanes = a.slot_count >= 32 ? 32 : a.slot_count;
+  Triple node = identity_triple();
+  if (lane < lanes) {
+    Triple stack[kMaxTreeDepth];
+    int sp = 0;
+    for (int q0 = 0; q0 < per; q0 += 8) {
+      Triple buf[8];
 #pragma unroll
-    for (int i = 0; i < kPrefetch; ++i) {
-      const int slot = a.slot_begin + q0 + i;
-      const int ss = slot / a.P, jj = slot - ss * a.P;
-      const int leaf = ss * a.L_ss + jj;
-      const int ll = leaf - a.leaf0;
-      buf[i] = identity_triple();
-      if (q0 + i < a.slot_count && jj < a.L_ss && leaf < a.n_leaves_global && ll >= 0 &&
-          ll < a.n_leaves_local) {
-        const size_t o = static_cast<size_t>(ll) * a.T + t;
-        buf[i] = Triple{a.ws_m[o], a.ws_s[o], a.ws_zt[o]};
+      for (int i = 0; i < 8; ++i)
+        buf[i] = (q0 + i < per) ? load_slot(a, t, lane * per + q0 + i) : identity_triple();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int q = q0 + i;
+        if (q >= per) break;
+        Triple n = buf[i];
+        for (int idx = q; idx & 1; idx >>= 1) n = merge_pair(stack[--sp], n);
+        stack[sp++] = n;
       }
     }
-#pragma unroll
-    for (int i = 0; i < kPrefetch; ++i) {
-      const int q = q0 + i;
-      if (q >= a.slot_count) break;
-      Triple node = buf[i];
-      for (int idx = q; idx & 1; idx >>= 1) node = merge_pair(stack[--sp], node);
-      stack[sp++] = node;
-    }
+    node = stack[0];
   }
-  Triple r = stack[0];
+  for (int d = 1; d < lanes; d <<= 1) {
+    const Triple other = shfl_xor_triple(node, d);
+    node = (lane & d) ? merge_pair(other, node) : merge_pair(node, other);
+  }
+  if (lane != 0) return;
+  Triple r = node;
   const int64_t y = a.y[t];
   if (y < 0 || y >= a.V_true) {
     r.zt = __int_as_float(0x7fc00000);
@@ -369,9 +387,7 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
     if (workspace_bytes < 3 * arr) return RLK_ERR_WORKSPACE;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float* ws_m = static_cast<float*>(workspace);
-  float* ws_s = reinterpret_cast<float*>(static_cast<char*>(workspace) + arr);
-  float* ws_zt = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * arr);
+  float* ws = static_cast<float*>(workspace);  // [T][n_leaves_local][3] (fits in 3 * arr)
 
   if (g.n_leaves_local > 0) {
     CUtensorMap tmA, tmB;
@@ -389,9 +405,7 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
     a.n_items = a.n_pm * a.n_leaves;
     a.n_kb = static_cast<int32_t>(ceil_div(H, BK));
     a.y = y;
-    a.ws_m = ws_m;
-    a.ws_s = ws_s;
-    a.ws_zt = ws_zt;
+    a.ws = ws;
     a.z_out = z_saved;
     a.z_ld = round_up(V_local, BN);
     a.err_flag = err_flag;
@@ -399,9 +413,7 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
   }
 
   TreeArgs ta;
-  ta.ws_m = ws_m;
-  ta.ws_s = ws_s;
-  ta.ws_zt = ws_zt;
+  ta.ws = ws;
   ta.T = static_cast<int32_t>(T);
   ta.n_leaves_local = static_cast<int32_t>(g.n_leaves_local);
   ta.leaf0 = static_cast<int32_t>(g.leaf0);
@@ -416,8 +428,8 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
   ta.logp = logp;
   ta.lse = lse;
   ta.err_flag = err_flag;
-  const int threads = 128;
-  leaf_tree_kernel<<<static_cast<unsigned>(ceil_div(T, threads)), threads, 0, s>>>(ta);
+  const int warps_per_block = 8;  // one warp per token
+  leaf_tree_kernel<<<static_cast<unsigned>(ceil_div(T, warps_per_block)), 32 * warps_per_block, 0, s>>>(ta);
   return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
 }
 

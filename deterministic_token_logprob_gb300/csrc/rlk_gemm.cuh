@@ -452,10 +452,10 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
     if constexpr (MODE == MODE_FWD) {
       if (ok && t < a.T) {
         const int leaf_local = item / a.n_pm;
-        const size_t o = static_cast<size_t>(leaf_local) * a.T + t;
-        a.ws_m[o] = st.m;
-        a.ws_s[o] = st.s;
-        a.ws_zt[o] = st.zt;
+        float* o = a.ws + (static_cast<size_t>(t) * a.n_leaves + leaf_local) * 3;
+        o[0] = st.m;
+        o[1] = st.s;
+        o[2] = st.zt;
       }
     }
   }
@@ -539,8 +539,6 @@ template <int MODE>
 cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
                         cudaStream_t stream) {
   auto kernel = gemm_kernel<MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = PAIR;
@@ -552,13 +550,16 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Ge
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // Resident pairs of this kernel on the current device (queried once per device).
+  // Shared-memory opt-in and resident pairs of this kernel, once per device (both
+  // are properties of the device; racing first calls compute the same values).
   static int resident[64] = {};
   int dev = 0;
-  e = cudaGetDevice(&dev);
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   int clusters = dev < 64 ? resident[dev] : 0;
   if (clusters <= 0) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(PAIR, 1, 1);
     e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
     if (e != cudaSuccess) return e;

@@ -50,9 +50,7 @@ struct GemmArgs {
   int32_t n_pm = 0;                // fwd / dz: 256-token pair tiles
   int32_t leaf0 = 0, n_leaves = 0; // fwd: global index of the shard's first leaf, leaf count
   const int64_t* y = nullptr;
-  float* ws_m = nullptr;           // fwd: [n_leaves][T]
-  float* ws_s = nullptr;
-  float* ws_zt = nullptr;
+  float* ws = nullptr;             // fwd: (m, s, zt) per (token, leaf), [T][n_leaves][3]
   float* z_out = nullptr;          // fwd, optional: fp32 logits [T][z_ld] (local columns)
   int64_t z_ld = 0;
   const float* lse = nullptr;      // dz
