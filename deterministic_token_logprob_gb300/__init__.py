@@ -11,4 +11,4 @@ from ._binding import (  # noqa: F401
     RLK_ERR_WORKSPACE, RLK_FLAG_BAD_TARGET, RLK_FLAG_TIMEOUT, RLK_OK, RlkError,
     bwd_workspace_bytes, fwd_workspace_bytes, lib, library_path, linear_logp_bwd,
     linear_logp_bwd_saved, linear_logp_fwd, linear_logp_fwd_save, lse_merge, saved_logits_buffer,
-    saved_logits_bytes, shard_bounds, shard_sum_bf16, version)
+    saved_logits_bytes, selftest_wait_timeout, shard_bounds, shard_sum_bf16, version)

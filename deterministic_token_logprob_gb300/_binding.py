@@ -73,6 +73,8 @@ def _load():
         lib.rlk_linear_logp_bwd_saved.argtypes = [P, P, P, P, P, P, SZ, I64, I64, I64, I64, I64, P,
                                                   I32, P, P, P, SZ, P]
         lib.rlk_linear_logp_bwd_saved.restype = ctypes.c_int
+        lib.rlk_selftest_wait_timeout.argtypes = [P, P, P, I64, I64, I64, I64, P, P, P, P, SZ, P]
+        lib.rlk_selftest_wait_timeout.restype = ctypes.c_int
         lib.rlk_shard_sum_bf16.argtypes = [P, I32, I64, P, P]
         lib.rlk_shard_sum_bf16.restype = ctypes.c_int
         lib.rlk_status_string.argtypes = [ctypes.c_int]
@@ -324,6 +326,25 @@ def linear_logp_bwd_saved(h: torch.Tensor, W: torch.Tensor, y: torch.Tensor, lse
         _ptr(err_flag), _ptr(ws), nbytes, _stream_handle(stream))
     _check("rlk_linear_logp_bwd_saved", st)
     return dH, dW
+
+
+def selftest_wait_timeout(h: torch.Tensor, W: torch.Tensor, y: torch.Tensor, V_true: int,
+                          err_flag: torch.Tensor, stream=None) -> None:
+    """rlk_selftest_wait_timeout: a forward whose first pipeline wait is made to run
+    out; afterwards (once the stream is synchronised) err_flag holds RLK_FLAG_TIMEOUT."""
+    _need(h, "h", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 2)
+    _need(y, "y", torch.int64, 1)
+    _need(err_flag, "err_flag", torch.int32, 1)
+    T, H = h.shape
+    V = W.shape[0]
+    ws = _workspace(fwd_workspace_bytes(T, H, V), h.device, None)
+    logp = torch.empty(T, dtype=torch.float32, device=h.device)
+    lse = torch.empty(T, dtype=torch.float32, device=h.device)
+    st = _load().rlk_selftest_wait_timeout(_ptr(h), _ptr(W), _ptr(y), T, H, V, int(V_true),
+                                           _ptr(logp), _ptr(lse), _ptr(err_flag), _ptr(ws),
+                                           ws.numel(), _stream_handle(stream))
+    _check("rlk_selftest_wait_timeout", st)
 
 
 def shard_sum_bf16(partials: torch.Tensor, *, out: Optional[torch.Tensor] = None, stream=None):

@@ -370,7 +370,8 @@ namespace {
 rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, int64_t H,
                     int64_t V_local, int64_t vocab_start, int64_t V_true, float* logp, float* lse,
                     rlk_lse_partial* partial, float* z_saved, size_t z_saved_bytes,
-                    int32_t* err_flag, void* workspace, size_t workspace_bytes, void* stream) {
+                    int32_t* err_flag, void* workspace, size_t workspace_bytes, void* stream,
+                    int32_t stall_stage = -1) {
   rlk_status st = common_checks(h, W, y, T, H, V_local, vocab_start, V_true);
   if (st != RLK_OK) return st;
   if (T > 0 && !partial && !logp && !lse) return RLK_ERR_INVALID_ARG;
@@ -409,6 +410,7 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
     a.z_out = z_saved;
     a.z_ld = round_up(V_local, BN);
     a.err_flag = err_flag;
+    a.stall_stage = stall_stage;
     if (launch_gemm_fwd(tmA, tmB, a, s) != cudaSuccess) return RLK_ERR_CUDA;
   }
 
@@ -448,6 +450,15 @@ rlk_status rlk_linear_logp_fwd(const void* h, const void* W, const int64_t* y, i
 }
 
 size_t rlk_saved_logits_bytes(int64_t T, int64_t V_local) { return saved_logits_bytes(T, V_local); }
+
+rlk_status rlk_selftest_wait_timeout(const void* h, const void* W, const int64_t* y, int64_t T,
+                                     int64_t H, int64_t V, int64_t V_true, float* logp, float* lse,
+                                     int32_t* err_flag, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  if (!err_flag || T <= 0) return RLK_ERR_INVALID_ARG;
+  return fwd_impl(h, W, y, T, H, V, 0, V_true, logp, lse, nullptr, nullptr, 0, err_flag, workspace,
+                  workspace_bytes, stream, /*stall_stage=*/0);
+}
 
 rlk_status rlk_linear_logp_fwd_save(const void* h, const void* W, const int64_t* y, int64_t T,
                                     int64_t H, int64_t V_local, int64_t vocab_start,

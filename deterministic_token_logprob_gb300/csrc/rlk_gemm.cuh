@@ -158,6 +158,10 @@ __device__ void producer_loop(const CUtensorMap* tmA, const CUtensorMap* tmB, co
         uint8_t* sB = sA + A_STAGE_BYTES;
         const uint32_t bar = map_to_cta(smem_u32(&full[s]), 0);  // the even CTA's barrier
         if (r == 0) mbar_arrive_expect_tx(&full[s], tx);
+        if (r == 0 && static_cast<int32_t>(issued) == a.stall_stage) {
+          ++issued;  // self-test: this stage's bytes never arrive
+          continue;
+        }
         const int k0 = kb * BK;
         if constexpr (kAPerRow) {
           for (int q = 0; q < boxes_mine; ++q)            // h / dz, K-major boxes 64 x 64

@@ -63,6 +63,9 @@ struct GemmArgs {
   int32_t out_rows = 0, out_cols = 0;
   int32_t out_f32 = 0;
   int32_t n_mt = 0, n_nt = 0;      // dH / dW: 256-row pair tiles along M, 256-column tiles along N
+  // Self-test only (rlk_selftest_wait_timeout): the even CTA arms its `stall_stage`-th
+  // stage but issues none of its copies, so the wait on that stage cannot complete.
+  int32_t stall_stage = -1;
 };
 
 // Launchers (one translation unit each): enqueue one cluster launch (pairs of CTAs,

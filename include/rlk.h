@@ -249,6 +249,22 @@ RLK_API rlk_status rlk_linear_logp_fwd_noalloc(const void* h, const void* W, con
                                                float* lse, rlk_lse_partial* partial,
                                                int32_t* err_flag, void* stream);
 
+/*
+ * Self-test of the kernels' bounded waits. Runs the unsharded forward (arguments
+ * as rlk_linear_logp_fwd with vocab_start = 0) with the first shared-memory stage
+ * of one CTA deliberately left unfilled, so the pipeline's first wait can never
+ * complete. After the wait limit (2 s) the kernel gives up: it raises its abort
+ * flag in both CTAs of the pair, drains the copies and tensor-core work already in
+ * flight, frees its tensor memory, ORs RLK_FLAG_TIMEOUT into *err_flag (required)
+ * and returns; the kernel takes about 4 s and logp / lse are undefined. No fault,
+ * trap or hang is involved, and the CUDA context stays usable afterwards.
+ */
+RLK_API rlk_status rlk_selftest_wait_timeout(const void* h, const void* W, const int64_t* y,
+                                             int64_t T, int64_t H, int64_t V, int64_t V_true,
+                                             float* logp, float* lse, int32_t* err_flag,
+                                             void* workspace, size_t workspace_bytes,
+                                             void* stream);
+
 /* Static description of a status code. */
 RLK_API const char* rlk_status_string(rlk_status s);
 
