@@ -330,6 +330,16 @@ size_t fwd_ws_array_bytes(int64_t T, int64_t V_local) {
   return static_cast<size_t>(round_up(ceil_div(V_local, LEAF) * T * 4, 256));
 }
 
+// Backward workspace: the bf16 dz tiles, then (when dH's K = vocab spans several
+// accumulation chunks) an fp32 running sum for a bf16 dH.
+size_t bwd_dz_bytes(int64_t T, int64_t V_local) {
+  return static_cast<size_t>(round_up(T * round_up(V_local, BN) * 2, 256));
+}
+
+size_t bwd_run_bytes(int64_t T, int64_t H, int64_t V_local) {
+  return V_local > static_cast<int64_t>(KC_BLOCKS) * BK ? static_cast<size_t>(T) * H * 4 : 0;
+}
+
 size_t saved_logits_bytes(int64_t T, int64_t V_local) {
   if (T <= 0 || V_local <= 0) return 0;
   return static_cast<size_t>(T) * static_cast<size_t>(round_up(V_local, BN)) * 4;
@@ -484,9 +494,8 @@ rlk_status rlk_lse_merge(const rlk_lse_partial* partials, int32_t S, int64_t T, 
 }
 
 size_t rlk_linear_logp_bwd_workspace(int64_t T, int64_t H, int64_t V_local) {
-  (void)H;
   if (T <= 0 || V_local <= 0) return 0;
-  return static_cast<size_t>(T) * static_cast<size_t>(round_up(V_local, BN)) * 2;
+  return bwd_dz_bytes(T, V_local) + bwd_run_bytes(T, H, V_local);
 }
 
 }  // extern "C"
@@ -569,6 +578,8 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
       a.out_rows = static_cast<int32_t>(T);
       a.out_cols = static_cast<int32_t>(H);
       a.out_f32 = dH_fp32_partial ? 1 : 0;
+      if (!dH_fp32_partial && a.n_kb > KC_BLOCKS)
+        a.acc_scratch = reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_dz_bytes(T, V_local));
       a.err_flag = err_flag;
       if (launch_gemm_dh(tmA, tmB, a, s) != cudaSuccess) return RLK_ERR_CUDA;
     }

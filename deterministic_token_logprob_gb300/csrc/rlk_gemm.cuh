@@ -55,6 +55,13 @@ __device__ __forceinline__ int item_tiles(const GemmArgs& a, int item) {
   }
 }
 
+// Accumulator chunks per tile: dH / dW split K into KC_BLOCKS-block chunks.
+template <int MODE>
+__device__ __forceinline__ int tile_chunks(const GemmArgs& a) {
+  if constexpr (MODE == MODE_DH || MODE == MODE_DW) return (a.n_kb + KC_BLOCKS - 1) / KC_BLOCKS;
+  return 1;
+}
+
 // Pair-tile origin: m0 = first of the pair's 256 A / accumulator rows, n0 = first
 // of its 256 B rows (fwd/dz: local W row; dH/dW: output column).
 template <int MODE>
@@ -213,8 +220,9 @@ __device__ void mma_loop(const GemmArgs& a, uint8_t* smem, uint64_t* full, uint6
   using Ops = Operands<MODE>;
   uint32_t it = 0, tile = 0;
   bool ok = true;
+  const int nchunks = tile_chunks<MODE>(a);
   for (int item = c.cluster; ok && item < a.n_items; item += c.n_clusters) {
-    const int ntiles = item_tiles<MODE>(a, item);
+    const int ntiles = item_tiles<MODE>(a, item) * nchunks;  // accumulator fills of this item
     for (int j = 0; ok && j < ntiles; ++j) {
       const uint32_t buf = tile & 1u, use = tile >> 1;
       if (!pair_wait(&acc_empty[buf], (use & 1u) ^ 1u, c)) {
@@ -223,7 +231,10 @@ __device__ void mma_loop(const GemmArgs& a, uint8_t* smem, uint64_t* full, uint6
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + buf * BN;
-      for (int kb = 0; kb < a.n_kb; ++kb, ++it) {
+      const int chunk = j % nchunks;
+      const int kb_begin = chunk * KC_BLOCKS;
+      const int kb_end = nchunks == 1 ? a.n_kb : min(a.n_kb, kb_begin + KC_BLOCKS);
+      for (int kb = kb_begin; kb < kb_end; ++kb, ++it) {
         const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
         if (!pair_wait(&full[s], ph, c)) {
           ok = false;
@@ -238,7 +249,7 @@ __device__ void mma_loop(const GemmArgs& a, uint8_t* smem, uint64_t* full, uint6
                                         : make_smem_desc(a_base + k * 32, 16, 1024);
           const uint64_t bd = Ops::B_MN ? make_smem_desc(b_base + k * 2048, MN_ATOM_BYTES, 1024)
                                         : make_smem_desc(b_base + k * 32, 16, 1024);
-          umma_bf16_pair(d_tmem, ad, bd, Ops::IDESC, (kb | k) != 0 ? 1u : 0u);
+          umma_bf16_pair(d_tmem, ad, bd, Ops::IDESC, (kb != kb_begin || k != 0) ? 1u : 0u);
         }
         umma_commit_pair_multicast(&empty[s], 0x3);  // stage s free in both CTAs
       }
@@ -328,8 +339,9 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
   uint32_t tile = 0;
   bool ok = true;
 
+  const int nchunks = tile_chunks<MODE>(a);
   for (int item = c.cluster; ok && item < a.n_items; item += c.n_clusters) {
-    const int ntiles = item_tiles<MODE>(a, item);
+    const int ntiles = item_tiles<MODE>(a, item) * nchunks;  // accumulator fills of this item
     int m0, n0;
     tile_origin<MODE>(a, item, 0, m0, n0);
 
@@ -420,13 +432,40 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
           }
         }
       } else {
-        // dH / dW: plain stores of the fp32 accumulator (bf16 for dH unless partial)
+        // dH / dW: chunk j of nchunks. With one chunk the accumulator is stored directly
+        // (bf16 for dH unless partial); otherwise chunk sums go to an fp32 running sum
+        // (the fp32 output itself, or the scratch for a bf16 dH), folded in ascending
+        // chunk order with round-to-nearest adds, and the last chunk writes the output.
         const bool row_ok = t < a.out_rows;
+        const bool first = j == 0, last = j == nchunks - 1;
+        float* run = a.out_f32 ? static_cast<float*>(a.out) : a.acc_scratch;
 #pragma unroll 1
         for (int ch = 0; ch < BN; ch += 64) {
           float v[64];
           tmem_ld64(taddr + ch, v);
           const int col = n0 + ch;
+          if (row_ok && col < a.out_cols && nchunks > 1) {
+            float* p = run + static_cast<size_t>(t) * a.out_ld + col;
+            if (!first) {
+#pragma unroll
+              for (int q = 0; q < 16; ++q)
+                if (col + 4 * q < a.out_cols) {
+                  const float4 r = *reinterpret_cast<const float4*>(p + 4 * q);
+                  v[4 * q] = __fadd_rn(r.x, v[4 * q]);
+                  v[4 * q + 1] = __fadd_rn(r.y, v[4 * q + 1]);
+                  v[4 * q + 2] = __fadd_rn(r.z, v[4 * q + 2]);
+                  v[4 * q + 3] = __fadd_rn(r.w, v[4 * q + 3]);
+                }
+            }
+            if (!last) {
+#pragma unroll
+              for (int q = 0; q < 16; ++q)
+                if (col + 4 * q < a.out_cols)
+                  *reinterpret_cast<float4*>(p + 4 * q) =
+                      make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+              continue;
+            }
+          }
           if (row_ok && col < a.out_cols) {
             if (a.out_f32) {
               float* p = static_cast<float*>(a.out) + static_cast<size_t>(t) * a.out_ld + col;

@@ -17,6 +17,12 @@ constexpr int UMMA_K = 16;   // K of one tcgen05.mma kind::f16
 constexpr int LEAF = 1024;   // vocab columns per leaf of the merge tree
 constexpr int TILES_PER_LEAF = LEAF / BN;
 constexpr int MAX_SHARDS = 8;
+// dH / dW reduce over the vocabulary / the tokens, which can be very long. The tensor
+// core accumulates with truncation, a bias that grows with the number of accumulation
+// steps, so these two contractions restart the TMEM accumulator every KC_BLOCKS k-blocks
+// (K = 16384) and the epilogue folds the chunk results in ascending order with
+// round-to-nearest fp32 adds. The chunking depends only on K.
+constexpr int KC_BLOCKS = 256;
 
 // A CTA pair (cluster of 2, tcgen05 cta_group::2) computes one 256 x 256 tile: CTA r
 // holds rows [128 r, 128 r + 128) of A and of the accumulator, and rows
@@ -62,6 +68,7 @@ struct GemmArgs {
   int64_t out_ld = 0;
   int32_t out_rows = 0, out_cols = 0;
   int32_t out_f32 = 0;
+  float* acc_scratch = nullptr;    // dH with bf16 output and several K chunks: fp32 running sum, ld = out_ld
   int32_t n_mt = 0, n_nt = 0;      // dH / dW: 256-row pair tiles along M, 256-column tiles along N
   // Self-test only (rlk_selftest_wait_timeout): the even CTA arms its `stall_stage`-th
   // stage but issues none of its copies, so the wait on that stage cannot complete.

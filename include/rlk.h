@@ -158,7 +158,8 @@ RLK_API rlk_status rlk_lse_merge(const rlk_lse_partial* partials, int32_t S, int
 
 /* Bytes of device workspace rlk_linear_logp_bwd needs: the bf16 dz tile store
  * [T][round_up(V_local, 256)] (the "controlled workspace" of the fourth reason
- * in "Why the Fused Path Wins"). */
+ * in "Why the Fused Path Wins"), plus, when V_local > 16384, an fp32 [T][H]
+ * running sum for dH's chunked accumulation. */
 RLK_API size_t rlk_linear_logp_bwd_workspace(int64_t T, int64_t H, int64_t V_local);
 
 /*
@@ -175,7 +176,11 @@ RLK_API size_t rlk_linear_logp_bwd_workspace(int64_t T, int64_t H, int64_t V_loc
  * dz[t][v] = g[t] (1[v == y[t]] - exp(z[t][v] - lse[t])) is recomputed from a
  * fresh z tile with the forward's exact tensor-core sequence, rounded once to
  * bf16; dH = dz W sums the vocabulary in ascending 64-column steps, dW = dz^T h
- * sums the tokens in ascending 64-row steps, each output tile by one CTA.
+ * sums the tokens in ascending 64-row steps, each output tile by one CTA pair.
+ * Both reductions run in fixed chunks of 16384 (tensor-core fp32 accumulation
+ * within a chunk, then round-to-nearest fp32 adds of the chunk results in
+ * ascending order), which keeps the accumulation bias of very long reductions
+ * bounded; the chunking depends on neither T's batch composition nor the launch.
  */
 RLK_API rlk_status rlk_linear_logp_bwd(const void* h, const void* W, const int64_t* y, const float* lse,
                                const float* g, int64_t T, int64_t H, int64_t V_local,

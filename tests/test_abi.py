@@ -60,8 +60,9 @@ def test_workspace_queries(lib):
     T, V = 4096, 151936
     per = -(-(V // 1024 + (V % 1024 > 0)) * T * 4 // 256) * 256
     assert lib.rlk_linear_logp_fwd_workspace(T, 4096, V) == 3 * per
-    # backward: bf16 dz tiles [T][round_up(V_local, 256)]
-    assert lib.rlk_linear_logp_bwd_workspace(T, 4096, V) == T * 152064 * 2
+    # backward: bf16 dz tiles [T][round_up(V_local, 256)] + fp32 [T][H] running sum of dH
+    assert lib.rlk_linear_logp_bwd_workspace(T, 4096, V) == T * 152064 * 2 + T * 4096 * 4
+    assert lib.rlk_linear_logp_bwd_workspace(T, 4096, 16384) == T * 16384 * 2  # one chunk
     assert lib.rlk_linear_logp_fwd_workspace(0, 4096, V) == 0
     assert lib.rlk_linear_logp_bwd_workspace(0, 4096, V) == 0
 
