@@ -367,6 +367,7 @@ def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int)
         if w.name == "qwen3_8b":  # legs defined on the Qwen3-8B weight
             line["fwd_only"] = fwd_only(rlk, torch, W_bits, path, device, args, peak)
             line["saved_logits"] = saved_logits_leg(rlk, torch, path, wr, device, args, peak, peak_sus)
+            line["saved_probs_bf16"] = saved_probs_leg(rlk, torch, path, wr, device, args, peak)
             line["small_T_forward"] = small_t_leg(rlk, torch, path, device, peaks)
         line["e2e"] = e2e(rlk, torch, path, wr, d, device, args)
         rate, cores, sample = oracle_sample_rate(wr, d)
@@ -438,6 +439,34 @@ def small_t_leg(rlk, torch, path, device, peaks):
         out[str(T)] = {"us_per_call": ms * 1e3, "algorithmic_GBps": gbs, "frac_of_hbm": gbs / hbm}
     out["note"] = "W and L2 are not flushed between calls; W (1.24 GB) exceeds L2 on its own"
     return out
+
+
+def saved_probs_leg(rlk, torch, path, w, device, args, peak):
+    """The fwd+bwd step through the saved bf16-probabilities pair."""
+    pbuf = torch.empty(rlk.saved_probs_bytes(w.T, w.V), dtype=torch.uint8, device=device)
+
+    def step():
+        rlk.linear_logp_fwd_save_probs(path.h, path.W, path.y, w.V_true, p_saved=pbuf,
+                                       out=(path.logp, path.lse), workspace=path.fws)
+        rlk.linear_logp_bwd_saved_probs(path.h, path.W, path.y, path.lse, path.g, pbuf, w.V_true,
+                                        out=(path.dH, path.dW), workspace=path.bws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(device)
+    K = args.steps
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(K):
+        step()
+    b.record()
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / K
+    del pbuf
+    step_flops = 3.0 * 2.0 * w.T * w.H * w.V_true
+    return {"tokens_per_s": w.T / (ms / 1e3), "ms_per_step": ms,
+            "frac_of_burst": step_flops / (peak * 1e12) / (ms / 1e3),
+            "saved_probs_bytes": rlk.saved_probs_bytes(w.T, w.V), "steps": K}
 
 
 def fwd_only(rlk, torch, W_bits, path, device, args, peak):

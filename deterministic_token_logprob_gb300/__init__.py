@@ -10,5 +10,6 @@ from ._binding import (  # noqa: F401
     LEAF_WIDTH, MAX_SHARDS, RLK_ERR_CUDA, RLK_ERR_INVALID_ARG, RLK_ERR_UNSUPPORTED,
     RLK_ERR_WORKSPACE, RLK_FLAG_BAD_TARGET, RLK_FLAG_TIMEOUT, RLK_OK, RlkError,
     bwd_workspace_bytes, fwd_workspace_bytes, lib, library_path, linear_logp_bwd,
-    linear_logp_bwd_saved, linear_logp_fwd, linear_logp_fwd_save, lse_merge, saved_logits_buffer,
-    saved_logits_bytes, selftest_wait_timeout, shard_bounds, shard_sum_bf16, version)
+    linear_logp_bwd_saved, linear_logp_bwd_saved_probs, linear_logp_fwd, linear_logp_fwd_save,
+    linear_logp_fwd_save_probs, lse_merge, saved_logits_buffer, saved_logits_bytes, saved_probs_bytes,
+    selftest_wait_timeout, shard_bounds, shard_sum_bf16, version)

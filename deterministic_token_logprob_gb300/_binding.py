@@ -73,6 +73,14 @@ def _load():
         lib.rlk_linear_logp_bwd_saved.argtypes = [P, P, P, P, P, P, SZ, I64, I64, I64, I64, I64, P,
                                                   I32, P, P, P, SZ, P]
         lib.rlk_linear_logp_bwd_saved.restype = ctypes.c_int
+        lib.rlk_saved_probs_bytes.argtypes = [I64, I64]
+        lib.rlk_saved_probs_bytes.restype = SZ
+        lib.rlk_linear_logp_fwd_save_probs.argtypes = [P, P, P, I64, I64, I64, I64, I64, P, P, P, P,
+                                                       SZ, P, P, SZ, P]
+        lib.rlk_linear_logp_fwd_save_probs.restype = ctypes.c_int
+        lib.rlk_linear_logp_bwd_saved_probs.argtypes = [P, P, P, P, P, P, SZ, I64, I64, I64, I64,
+                                                        I64, P, I32, P, P, P, SZ, P]
+        lib.rlk_linear_logp_bwd_saved_probs.restype = ctypes.c_int
         lib.rlk_selftest_wait_timeout.argtypes = [P, P, P, I64, I64, I64, I64, P, P, P, P, SZ, P]
         lib.rlk_selftest_wait_timeout.restype = ctypes.c_int
         lib.rlk_shard_sum_bf16.argtypes = [P, I32, I64, P, P]
@@ -325,6 +333,81 @@ def linear_logp_bwd_saved(h: torch.Tensor, W: torch.Tensor, y: torch.Tensor, lse
         V_local, int(vocab_start), int(V_true), _ptr(dH), 1 if dH_fp32_partial else 0, _ptr(dW),
         _ptr(err_flag), _ptr(ws), nbytes, _stream_handle(stream))
     _check("rlk_linear_logp_bwd_saved", st)
+    return dH, dW
+
+
+def saved_probs_bytes(T: int, V_local: int) -> int:
+    return int(_load().rlk_saved_probs_bytes(T, V_local))
+
+
+def linear_logp_fwd_save_probs(h: torch.Tensor, W: torch.Tensor, y: torch.Tensor, V_true: int, *,
+                               vocab_start: int = 0, partial: bool = False,
+                               p_saved: Optional[torch.Tensor] = None,
+                               out: Optional[Sequence[torch.Tensor]] = None,
+                               err_flag: Optional[torch.Tensor] = None,
+                               workspace: Optional[torch.Tensor] = None, stream=None):
+    """rlk_linear_logp_fwd_save_probs: the forward that also stores bf16 probabilities
+    (and their fp32 chunk maxima) in one byte buffer. Returns ((logp, lse) or partial, p_saved)."""
+    _need(h, "h", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 2)
+    _need(y, "y", torch.int64, 1)
+    T, H = h.shape
+    V_local = W.shape[0]
+    dev = h.device
+    if p_saved is None:
+        p_saved = torch.empty(max(1, saved_probs_bytes(T, V_local)), dtype=torch.uint8, device=dev)
+    _need(p_saved, "p_saved", torch.uint8, 1)
+    ws = _workspace(fwd_workspace_bytes(T, H, V_local), dev, workspace)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    if partial:
+        p = out[0] if out is not None else torch.empty((T, 3), dtype=torch.float32, device=dev)
+        logp = lse = None
+    else:
+        p = None
+        if out is not None:
+            logp, lse = out
+        else:
+            logp = torch.empty(T, dtype=torch.float32, device=dev)
+            lse = torch.empty(T, dtype=torch.float32, device=dev)
+    st = _load().rlk_linear_logp_fwd_save_probs(
+        _ptr(h), _ptr(W), _ptr(y), T, H, V_local, int(vocab_start), int(V_true), _ptr(logp),
+        _ptr(lse), _ptr(p), _ptr(p_saved), p_saved.numel(), _ptr(err_flag), _ptr(ws), nbytes,
+        _stream_handle(stream))
+    _check("rlk_linear_logp_fwd_save_probs", st)
+    return (p if partial else (logp, lse)), p_saved
+
+
+def linear_logp_bwd_saved_probs(h: torch.Tensor, W: torch.Tensor, y: torch.Tensor,
+                                lse: torch.Tensor, g: torch.Tensor, p_saved: torch.Tensor,
+                                V_true: int, *, vocab_start: int = 0,
+                                dH_fp32_partial: bool = False, want_dH: bool = True,
+                                want_dW: bool = True,
+                                out: Optional[Tuple[Optional[torch.Tensor], Optional[torch.Tensor]]] = None,
+                                err_flag: Optional[torch.Tensor] = None,
+                                workspace: Optional[torch.Tensor] = None, stream=None):
+    """rlk_linear_logp_bwd_saved_probs: the backward from saved bf16 probabilities -> (dH, dW)."""
+    _need(h, "h", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 2)
+    _need(y, "y", torch.int64, 1)
+    _need(lse, "lse", torch.float32, 1)
+    _need(g, "g", torch.float32, 1)
+    _need(p_saved, "p_saved", torch.uint8, 1)
+    T, H = h.shape
+    V_local = W.shape[0]
+    dev = h.device
+    if out is not None:
+        dH, dW = out
+    else:
+        dH = (torch.empty((T, H), dtype=torch.float32 if dH_fp32_partial else torch.bfloat16,
+                          device=dev) if want_dH else None)
+        dW = torch.empty((V_local, H), dtype=torch.float32, device=dev) if want_dW else None
+    ws = _workspace(bwd_workspace_bytes(T, H, V_local), dev, workspace)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    st = _load().rlk_linear_logp_bwd_saved_probs(
+        _ptr(h), _ptr(W), _ptr(y), _ptr(lse), _ptr(g), _ptr(p_saved), p_saved.numel(), T, H,
+        V_local, int(vocab_start), int(V_true), _ptr(dH), 1 if dH_fp32_partial else 0, _ptr(dW),
+        _ptr(err_flag), _ptr(ws), nbytes, _stream_handle(stream))
+    _check("rlk_linear_logp_bwd_saved_probs", st)
     return dH, dW
 
 

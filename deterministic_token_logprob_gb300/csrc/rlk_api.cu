@@ -237,6 +237,46 @@ __global__ void dz_from_logits_kernel(const float* z, int64_t z_ld, const int64_
   }
 }
 
+// dz from saved bf16 probabilities: p = e(z - m) (bf16) x e(m - lse), m the row's
+// running max recorded per 64-column chunk; eight consecutive columns per thread.
+__global__ void dz_from_probs_kernel(const uint16_t* pb, const float* pm, int64_t ld,
+                                     const int64_t* y, const float* lse, const float* g, int T,
+                                     int Vd, int V_valid, int vocab_start, int V_true,
+                                     uint16_t* dz, int64_t dz_ld, int32_t* err_flag) {
+  const int64_t groups = static_cast<int64_t>(Vd / 8);
+  const int64_t total = static_cast<int64_t>(T) * groups;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(idx / groups);
+    const int c0 = static_cast<int>(idx - static_cast<int64_t>(t) * groups) * 8;
+    const int64_t yt = y[t];
+    const bool yvalid = yt >= 0 && yt < V_true;
+    if (!yvalid && c0 == 0 && err_flag) atomicOr(err_flag, RLK_FLAG_BAD_TARGET);
+    float d[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d[i] = 0.f;
+    if (yvalid && c0 < V_valid) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(pb + static_cast<size_t>(t) * ld + c0);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      const float gt = g[t];
+      const float scale = exp_shifted(pm[static_cast<size_t>(t) * (ld / 64) + c0 / 64], neg_scaled(lse[t]));
+      const int64_t tl = yt - vocab_start - c0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t bits = (i & 1) ? (w[i >> 1] & 0xFFFF0000u) : (w[i >> 1] << 16);
+        const float p = __fmul_rn(__uint_as_float(bits), scale);
+        if (c0 + i < V_valid) d[i] = (i == tl) ? __fmul_rn(gt, __fsub_rn(1.f, p)) : __fmul_rn(-gt, p);
+      }
+    }
+    uint4 o;
+    o.x = pack_bf16x2(d[0], d[1]);
+    o.y = pack_bf16x2(d[2], d[3]);
+    o.z = pack_bf16x2(d[4], d[5]);
+    o.w = pack_bf16x2(d[6], d[7]);
+    *reinterpret_cast<uint4*>(dz + static_cast<size_t>(t) * dz_ld + c0) = o;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // host helpers
 // ---------------------------------------------------------------------------
@@ -340,6 +380,17 @@ size_t bwd_run_bytes(int64_t T, int64_t H, int64_t V_local) {
   return V_local > static_cast<int64_t>(KC_BLOCKS) * BK ? static_cast<size_t>(T) * H * 4 : 0;
 }
 
+// Saved probabilities: bf16 [T][round_up(V_local, 256)], then fp32 chunk maxima
+// [T][round_up(V_local, 256) / 64] at a 256-byte aligned offset.
+size_t saved_probs_offset(int64_t T, int64_t V_local) {
+  return static_cast<size_t>(round_up(T * round_up(V_local, BN) * 2, 256));
+}
+
+size_t saved_probs_bytes(int64_t T, int64_t V_local) {
+  if (T <= 0 || V_local <= 0) return 0;
+  return saved_probs_offset(T, V_local) + static_cast<size_t>(T) * (round_up(V_local, BN) / 64) * 4;
+}
+
 size_t saved_logits_bytes(int64_t T, int64_t V_local) {
   if (T <= 0 || V_local <= 0) return 0;
   return static_cast<size_t>(T) * static_cast<size_t>(round_up(V_local, BN)) * 4;
@@ -381,7 +432,7 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
                     int64_t V_local, int64_t vocab_start, int64_t V_true, float* logp, float* lse,
                     rlk_lse_partial* partial, float* z_saved, size_t z_saved_bytes,
                     int32_t* err_flag, void* workspace, size_t workspace_bytes, void* stream,
-                    int32_t stall_stage = -1) {
+                    int32_t stall_stage = -1, void* p_saved = nullptr, size_t p_saved_bytes = 0) {
   rlk_status st = common_checks(h, W, y, T, H, V_local, vocab_start, V_true);
   if (st != RLK_OK) return st;
   if (T > 0 && !partial && !logp && !lse) return RLK_ERR_INVALID_ARG;
@@ -390,6 +441,9 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
   if (st != RLK_OK) return st;
   if (!partial && (vocab_start != 0 || !g.reaches_end)) return RLK_ERR_INVALID_ARG;
   if (z_saved && (!aligned16(z_saved) || z_saved_bytes < saved_logits_bytes(T, V_local)))
+    return RLK_ERR_INVALID_ARG;
+  if (p_saved && ((reinterpret_cast<uintptr_t>(p_saved) & 255u) != 0 ||
+                  p_saved_bytes < saved_probs_bytes(T, V_local)))
     return RLK_ERR_INVALID_ARG;
   if (T == 0) return RLK_OK;
   const size_t arr = fwd_ws_array_bytes(T, V_local);
@@ -419,6 +473,10 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
     a.ws = ws;
     a.z_out = z_saved;
     a.z_ld = round_up(V_local, BN);
+    if (p_saved) {
+      a.p_out = static_cast<uint16_t*>(p_saved);
+      a.pm_out = reinterpret_cast<float*>(static_cast<char*>(p_saved) + saved_probs_offset(T, V_local));
+    }
     a.err_flag = err_flag;
     a.stall_stage = stall_stage;
     if (launch_gemm_fwd(tmA, tmB, a, s) != cudaSuccess) return RLK_ERR_CUDA;
@@ -460,6 +518,19 @@ rlk_status rlk_linear_logp_fwd(const void* h, const void* W, const int64_t* y, i
 }
 
 size_t rlk_saved_logits_bytes(int64_t T, int64_t V_local) { return saved_logits_bytes(T, V_local); }
+
+size_t rlk_saved_probs_bytes(int64_t T, int64_t V_local) { return saved_probs_bytes(T, V_local); }
+
+rlk_status rlk_linear_logp_fwd_save_probs(const void* h, const void* W, const int64_t* y,
+                                          int64_t T, int64_t H, int64_t V_local,
+                                          int64_t vocab_start, int64_t V_true, float* logp,
+                                          float* lse, rlk_lse_partial* partial, void* p_saved,
+                                          size_t p_saved_bytes, int32_t* err_flag,
+                                          void* workspace, size_t workspace_bytes, void* stream) {
+  if (T > 0 && !p_saved) return RLK_ERR_INVALID_ARG;
+  return fwd_impl(h, W, y, T, H, V_local, vocab_start, V_true, logp, lse, partial, nullptr, 0,
+                  err_flag, workspace, workspace_bytes, stream, -1, p_saved, p_saved_bytes);
+}
 
 rlk_status rlk_selftest_wait_timeout(const void* h, const void* W, const int64_t* y, int64_t T,
                                      int64_t H, int64_t V, int64_t V_true, float* logp, float* lse,
@@ -509,7 +580,7 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
                     const float* g, const float* z_saved, int64_t T, int64_t H, int64_t V_local,
                     int64_t vocab_start, int64_t V_true, void* dH, int32_t dH_fp32_partial,
                     float* dW, int32_t* err_flag, void* workspace, size_t workspace_bytes,
-                    void* stream) {
+                    void* stream, const void* p_saved = nullptr) {
   rlk_status st = common_checks(h, W, y, T, H, V_local, vocab_start, V_true);
   if (st != RLK_OK) return st;
   if (T > 0 && (!lse || !g)) return RLK_ERR_INVALID_ARG;
@@ -523,8 +594,19 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
   uint16_t* dz = static_cast<uint16_t*>(workspace);
   const int32_t n_pm = static_cast<int32_t>(ceil_div(T, PAIR_M));
 
-  // 1. dz (bf16) workspace: from the saved logits, or from recomputed z tiles
-  if (z_saved) {
+  // 1. dz (bf16) workspace: from saved probabilities, saved logits, or recomputed z tiles
+  if (p_saved) {
+    const int64_t V_valid = std::max<int64_t>(0, std::min<int64_t>(V_true - vocab_start, V_local));
+    const int64_t total = T * (Vd / 8);
+    const int threads = 256;
+    const int64_t blocks = std::min<int64_t>(ceil_div(total, threads), 1 << 20);
+    dz_from_probs_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(
+        static_cast<const uint16_t*>(p_saved),
+        reinterpret_cast<const float*>(static_cast<const char*>(p_saved) + saved_probs_offset(T, V_local)),
+        Vd, y, lse, g, static_cast<int>(T), static_cast<int>(Vd), static_cast<int>(V_valid),
+        static_cast<int>(vocab_start), static_cast<int>(V_true), dz, Vd, err_flag);
+    if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
+  } else if (z_saved) {
     const int64_t V_valid = std::max<int64_t>(0, std::min<int64_t>(V_true - vocab_start, V_local));
     const int64_t total = T * (Vd / 8);
     const int threads = 256;
@@ -632,6 +714,20 @@ rlk_status rlk_linear_logp_bwd_saved(const void* h, const void* W, const int64_t
     return RLK_ERR_INVALID_ARG;
   return bwd_impl(h, W, y, lse, g, z_saved, T, H, V_local, vocab_start, V_true, dH,
                   dH_fp32_partial, dW, err_flag, workspace, workspace_bytes, stream);
+}
+
+rlk_status rlk_linear_logp_bwd_saved_probs(const void* h, const void* W, const int64_t* y,
+                                           const float* lse, const float* g, const void* p_saved,
+                                           size_t p_saved_bytes, int64_t T, int64_t H,
+                                           int64_t V_local, int64_t vocab_start, int64_t V_true,
+                                           void* dH, int32_t dH_fp32_partial, float* dW,
+                                           int32_t* err_flag, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+  if (T > 0 && (!p_saved || (reinterpret_cast<uintptr_t>(p_saved) & 255u) != 0 ||
+                p_saved_bytes < saved_probs_bytes(T, V_local)))
+    return RLK_ERR_INVALID_ARG;
+  return bwd_impl(h, W, y, lse, g, nullptr, T, H, V_local, vocab_start, V_true, dH,
+                  dH_fp32_partial, dW, err_flag, workspace, workspace_bytes, stream, p_saved);
 }
 
 rlk_status rlk_shard_sum_bf16(const float* partials, int32_t S, int64_t n, void* out, void* stream) {

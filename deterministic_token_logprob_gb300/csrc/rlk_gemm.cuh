@@ -36,6 +36,9 @@
 namespace rlk {
 
 template <int MODE>
+constexpr bool is_fwd = (MODE == MODE_FWD || MODE == MODE_FWDP);
+
+template <int MODE>
 struct Operands {
   static constexpr bool A_MN = (MODE == MODE_DW);
   static constexpr bool B_MN = (MODE == MODE_DH || MODE == MODE_DW);
@@ -45,7 +48,7 @@ struct Operands {
 // Number of 256-wide tiles in a work item.
 template <int MODE>
 __device__ __forceinline__ int item_tiles(const GemmArgs& a, int item) {
-  if constexpr (MODE == MODE_FWD) {
+  if constexpr (is_fwd<MODE>) {
     const int leaf_local = item / a.n_pm;
     const int col0 = (a.leaf0 + leaf_local) * LEAF;
     const int end = min(col0 + LEAF, a.V_true);
@@ -66,7 +69,7 @@ __device__ __forceinline__ int tile_chunks(const GemmArgs& a) {
 // of its 256 B rows (fwd/dz: local W row; dH/dW: output column).
 template <int MODE>
 __device__ __forceinline__ void tile_origin(const GemmArgs& a, int item, int j, int& m0, int& n0) {
-  if constexpr (MODE == MODE_FWD) {
+  if constexpr (is_fwd<MODE>) {
     const int leaf_local = item / a.n_pm, pm = item % a.n_pm;
     m0 = pm * PAIR_M;
     n0 = (a.leaf0 + leaf_local) * LEAF + j * BN - a.vocab_start;
@@ -133,7 +136,7 @@ __device__ void producer_loop(const CUtensorMap* tmA, const CUtensorMap* tmB, co
   const uint64_t pol_keep = policy_evict_last();
   const uint64_t pol_norm = policy_evict_normal();
   const uint64_t pol_first = policy_evict_first();
-  constexpr bool kZ = (MODE == MODE_FWD || MODE == MODE_DZ);
+  constexpr bool kZ = (is_fwd<MODE> || MODE == MODE_DZ);
   constexpr bool kAPerRow = (MODE != MODE_DW);  // A rows are tokens (independent outputs)
   const uint64_t polA = kZ ? pol_keep : pol_norm;
   const uint64_t polB = (MODE == MODE_DW) ? pol_keep : (kZ ? pol_first : pol_norm);
@@ -174,7 +177,7 @@ __device__ void producer_loop(const CUtensorMap* tmA, const CUtensorMap* tmB, co
           for (int q = 0; q < boxes_mine; ++q)            // h / dz, K-major boxes 64 x 64
             tma_load_2d_pair(sA + q * A_BOX_BYTES, tmA, bar, k0, am + q * A_BOX_ROWS, polA);
         }
-        if constexpr (MODE == MODE_FWD || MODE == MODE_DZ) {
+        if constexpr (is_fwd<MODE> || MODE == MODE_DZ) {
           tma_load_2d_pair(sB, tmB, bar, k0, bn, polB);   // W, K-major box 64 x 128
         } else if constexpr (MODE == MODE_DH) {
 #pragma unroll
@@ -319,6 +322,39 @@ __device__ __forceinline__ void fwd_chunk(float (&v)[64], int valid, int tl, Row
   st.s = __fadd_rn(st.s, sum_exp64(v, st.nb));
 }
 
+// The same update, also leaving e(z - m) of the 64 values in v (m = the running max
+// after this chunk) so they can be saved. The sum is formed in the same order as
+// sum_exp64, so the statistics are identical to fwd_chunk's.
+__device__ __forceinline__ void fwd_chunk_keep_exps(float (&v)[64], int valid, int tl, RowStats& st) {
+  if (valid < 64) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+      if (i >= valid) v[i] = neg_inf();
+  }
+  if (__any_sync(0xffffffffu, tl >= 0 && tl < 64)) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+      if (i == tl) st.zt = v[i];
+  }
+  const float cm = max64(v);
+  if (cm > st.m) {
+    const float nb = neg_scaled(cm);
+    st.s = __fmul_rn(st.s, exp_shifted(st.m, nb));
+    st.m = cm;
+    st.nb = nb;
+  }
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = exp_shifted(v[i], st.nb);
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = v[i];
+#pragma unroll
+  for (int i = 8; i < 64; ++i) acc[i & 7] = __fadd_rn(acc[i & 7], v[i]);
+  const float a01 = __fadd_rn(acc[0], acc[1]), a23 = __fadd_rn(acc[2], acc[3]);
+  const float a45 = __fadd_rn(acc[4], acc[5]), a67 = __fadd_rn(acc[6], acc[7]);
+  st.s = __fadd_rn(st.s, __fadd_rn(__fadd_rn(a01, a23), __fadd_rn(a45, a67)));
+}
+
 __device__ __forceinline__ uint4 pack8_bf16(const float* v) {
   uint4 w;
   w.x = pack_bf16x2(v[0], v[1]);
@@ -351,7 +387,7 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
     float g_t = 0.f, nl = 0.f;
     bool yvalid = false;
     const int t = m0 + static_cast<int>(c.rank) * BM + row;  // token row (fwd, dz, dH) or vocab row (dW)
-    if constexpr (MODE == MODE_FWD) {
+    if constexpr (is_fwd<MODE>) {
       if (t < a.T) yt = a.y[t];
     } else if constexpr (MODE == MODE_DZ) {
       if (t < a.T) {
@@ -374,12 +410,13 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
       tc_fence_after();
       const uint32_t taddr = lane_base + buf * BN;
 
-      if constexpr (MODE == MODE_FWD) {
+      if constexpr (is_fwd<MODE>) {
         const int c0 = n0 + a.vocab_start + j * BN;  // global column of the tile's first column
         const int vcols = min(BN, a.V_true - c0);
         const int tl = (yt >= c0 && yt < static_cast<int64_t>(c0) + vcols) ? static_cast<int>(yt - c0) : -1;
-        float* zrow = (a.z_out && t < a.T)
-                          ? a.z_out + static_cast<size_t>(t) * a.z_ld + (n0 + j * BN) : nullptr;
+        const size_t lc = static_cast<size_t>(n0 + j * BN);  // local column of the tile
+        float* zrow = (a.z_out && t < a.T) ? a.z_out + static_cast<size_t>(t) * a.z_ld + lc : nullptr;
+        constexpr bool keep_p = (MODE == MODE_FWDP);
 #pragma unroll 1
         for (int ch = 0; ch < BN; ch += 64) {
           float v[64];
@@ -392,7 +429,17 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
                                            __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3])),
                                 pol_out);
           }
-          fwd_chunk(v, vcols - ch, tl - ch, st);
+          if constexpr (keep_p) {  // saved probabilities: bf16 e(z - m) and the fp32 running max m
+            fwd_chunk_keep_exps(v, vcols - ch, tl - ch, st);
+            if (t < a.T) {
+              uint16_t* prow = a.p_out + static_cast<size_t>(t) * a.z_ld + lc + ch;
+#pragma unroll
+              for (int q = 0; q < 8; ++q) st_global_v4_hint(prow + 8 * q, pack8_bf16(v + 8 * q), pol_out);
+              a.pm_out[static_cast<size_t>(t) * (a.z_ld / 64) + (lc + ch) / 64] = st.m;
+            }
+          } else {
+            fwd_chunk(v, vcols - ch, tl - ch, st);
+          }
         }
       } else if constexpr (MODE == MODE_DZ) {
         const int gc0 = a.vocab_start + n0;
@@ -492,7 +539,7 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
       ++tile;
     }
 
-    if constexpr (MODE == MODE_FWD) {
+    if constexpr (is_fwd<MODE>) {
       if (ok && t < a.T) {
         const int leaf_local = item / a.n_pm;
         float* o = a.ws + (static_cast<size_t>(t) * a.n_leaves + leaf_local) * 3;

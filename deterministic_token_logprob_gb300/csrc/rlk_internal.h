@@ -19,10 +19,11 @@ constexpr int TILES_PER_LEAF = LEAF / BN;
 constexpr int MAX_SHARDS = 8;
 // dH / dW reduce over the vocabulary / the tokens, which can be very long. The tensor
 // core accumulates with truncation, a bias that grows with the number of accumulation
-// steps, so these two contractions restart the TMEM accumulator every KC_BLOCKS k-blocks
-// (K = 16384) and the epilogue folds the chunk results in ascending order with
-// round-to-nearest fp32 adds. The chunking depends only on K.
-constexpr int KC_BLOCKS = 256;
+// steps (measured: ~1e-4 relative after K = 65536), so these two contractions restart
+// the TMEM accumulator every KC_BLOCKS k-blocks (K = 65536) and the epilogue folds the
+// chunk results in ascending order with round-to-nearest fp32 adds. The chunking
+// depends only on K.
+constexpr int KC_BLOCKS = 1024;
 
 // A CTA pair (cluster of 2, tcgen05 cta_group::2) computes one 256 x 256 tile: CTA r
 // holds rows [128 r, 128 r + 128) of A and of the accumulator, and rows
@@ -44,6 +45,7 @@ enum GemmMode : int {
   MODE_DZ = 1,   // z = h W^T per tile: dz = g (onehot - p) -> bf16 workspace
   MODE_DH = 2,   // dH = dz W      (A K-major, B MN-major)
   MODE_DW = 3,   // dW = dz^T h    (A MN-major, B MN-major)
+  MODE_FWDP = 4, // MODE_FWD that also saves bf16 e(z - m) and the running maxima
 };
 
 struct GemmArgs {
@@ -59,6 +61,8 @@ struct GemmArgs {
   float* ws = nullptr;             // fwd: (m, s, zt) per (token, leaf), [T][n_leaves][3]
   float* z_out = nullptr;          // fwd, optional: fp32 logits [T][z_ld] (local columns)
   int64_t z_ld = 0;
+  uint16_t* p_out = nullptr;       // fwd, optional: bf16 e(z - m) [T][z_ld] with m the row's
+  float* pm_out = nullptr;         //   running max after each 64-column chunk, fp32 [T][z_ld / 64]
   const float* lse = nullptr;      // dz
   const float* g = nullptr;
   uint16_t* dz = nullptr;          // dz: bf16 bits [T][dz_ld]
@@ -78,7 +82,7 @@ struct GemmArgs {
 // Launchers (one translation unit each): enqueue one cluster launch (pairs of CTAs,
 // as many pairs as can be resident, at most one per work item) on `stream`.
 cudaError_t launch_gemm_fwd(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                            cudaStream_t stream);
+                            cudaStream_t stream);  // MODE_FWDP when a.p_out is set
 cudaError_t launch_gemm_dz(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
                            cudaStream_t stream);
 cudaError_t launch_gemm_dh(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,

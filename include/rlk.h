@@ -158,7 +158,7 @@ RLK_API rlk_status rlk_lse_merge(const rlk_lse_partial* partials, int32_t S, int
 
 /* Bytes of device workspace rlk_linear_logp_bwd needs: the bf16 dz tile store
  * [T][round_up(V_local, 256)] (the "controlled workspace" of the fourth reason
- * in "Why the Fused Path Wins"), plus, when V_local > 16384, an fp32 [T][H]
+ * in "Why the Fused Path Wins"), plus, when V_local > 65536, an fp32 [T][H]
  * running sum for dH's chunked accumulation. */
 RLK_API size_t rlk_linear_logp_bwd_workspace(int64_t T, int64_t H, int64_t V_local);
 
@@ -177,7 +177,7 @@ RLK_API size_t rlk_linear_logp_bwd_workspace(int64_t T, int64_t H, int64_t V_loc
  * fresh z tile with the forward's exact tensor-core sequence, rounded once to
  * bf16; dH = dz W sums the vocabulary in ascending 64-column steps, dW = dz^T h
  * sums the tokens in ascending 64-row steps, each output tile by one CTA pair.
- * Both reductions run in fixed chunks of 16384 (tensor-core fp32 accumulation
+ * Both reductions run in fixed chunks of 65536 (tensor-core fp32 accumulation
  * within a chunk, then round-to-nearest fp32 adds of the chunk results in
  * ascending order), which keeps the accumulation bias of very long reductions
  * bounded; the chunking depends on neither T's batch composition nor the launch.
@@ -219,6 +219,40 @@ RLK_API rlk_status rlk_linear_logp_bwd_saved(const void* h, const void* W, const
                                              int64_t V_true, void* dH, int32_t dH_fp32_partial,
                                              float* dW, int32_t* err_flag, void* workspace,
                                              size_t workspace_bytes, void* stream);
+
+/*
+ * Saved-probabilities variant (the bf16 "save probs" option of the pages'
+ * linear_logp settings, "Announcing RL-Kernel for vime", section "Quick Start"):
+ * the forward stores, for every logit, e(z - m) rounded to bf16 together with the
+ * row's fp32 running max m after each 64-column chunk, and the backward forms
+ * p = e(z - m) * e(m - lse) from them. Half the memory of the saved logits; dz
+ * carries an extra relative error of at most 2^-9 (bf16) per element, so dH / dW
+ * are NOT bit-identical to the recompute path (logp and lse are).
+ *
+ *   p_saved  device buffer of rlk_saved_probs_bytes(T, V_local) bytes, 256-byte
+ *            aligned, caller-owned: bf16 [T][round_up(V_local, 256)], then fp32
+ *            [T][round_up(V_local, 256) / 64] at a 256-byte aligned offset
+ * Every other argument is as in rlk_linear_logp_fwd / rlk_linear_logp_bwd.
+ */
+RLK_API size_t rlk_saved_probs_bytes(int64_t T, int64_t V_local);
+
+RLK_API rlk_status rlk_linear_logp_fwd_save_probs(const void* h, const void* W, const int64_t* y,
+                                                  int64_t T, int64_t H, int64_t V_local,
+                                                  int64_t vocab_start, int64_t V_true,
+                                                  float* logp, float* lse,
+                                                  rlk_lse_partial* partial, void* p_saved,
+                                                  size_t p_saved_bytes, int32_t* err_flag,
+                                                  void* workspace, size_t workspace_bytes,
+                                                  void* stream);
+
+RLK_API rlk_status rlk_linear_logp_bwd_saved_probs(const void* h, const void* W, const int64_t* y,
+                                                   const float* lse, const float* g,
+                                                   const void* p_saved, size_t p_saved_bytes,
+                                                   int64_t T, int64_t H, int64_t V_local,
+                                                   int64_t vocab_start, int64_t V_true, void* dH,
+                                                   int32_t dH_fp32_partial, float* dW,
+                                                   int32_t* err_flag, void* workspace,
+                                                   size_t workspace_bytes, void* stream);
 
 /*
  * out[i] = bf16(((p[0][i] + p[1][i]) + p[2][i]) + ...), the fixed ascending-order

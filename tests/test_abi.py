@@ -162,3 +162,19 @@ def test_saved_logits_queries_and_errors(lib):
     assert lib.rlk_linear_logp_bwd_saved(*bargs, FAKE, need - 1, *rest) == INVALID
     zero = (0, 64, 4096, 0, 4096, None, 0, None, None, None, 0, None)
     assert lib.rlk_linear_logp_bwd_saved(None, FAKE, None, None, None, None, 0, *zero) == OK
+
+
+def test_saved_probs_queries_and_errors(lib):
+    T, V = 8192, 151936
+    Vd = 152064
+    assert lib.rlk_saved_probs_bytes(T, V) == -(-T * Vd * 2 // 256) * 256 + T * (Vd // 64) * 4
+    need = lib.rlk_saved_probs_bytes(4, 4096)
+    args = (FAKE, FAKE, FAKE, 4, 64, 4096, 0, 4096, FAKE, FAKE, None)
+    assert lib.rlk_linear_logp_fwd_save_probs(*args, None, need, None, FAKE, 1 << 30, None) == INVALID
+    assert lib.rlk_linear_logp_fwd_save_probs(*args, FAKE, need - 1, None, FAKE, 1 << 30, None) == INVALID
+    assert lib.rlk_linear_logp_fwd_save_probs(*args, ctypes.c_void_p(0x100010), need, None, FAKE,
+                                              1 << 30, None) == INVALID      # not 256-aligned
+    bargs = (FAKE, FAKE, FAKE, FAKE, FAKE)
+    rest = (4, 64, 4096, 0, 4096, FAKE, 0, FAKE, None, FAKE, 1 << 30, None)
+    assert lib.rlk_linear_logp_bwd_saved_probs(*bargs, None, need, *rest) == INVALID
+    assert lib.rlk_linear_logp_bwd_saved_probs(*bargs, FAKE, need - 1, *rest) == INVALID

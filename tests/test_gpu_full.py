@@ -174,3 +174,22 @@ def test_qwen3_8b_saved_logits_bitwise(rlk, W8b):
     dH2, dW2 = rlk.linear_logp_bwd_saved(h, W, y, lse, g, z, w.V_true)
     assert torch.equal(dH, dH2)
     assert torch.equal(dW, dW2)
+
+
+def test_qwen3_8b_saved_probs_close_to_recompute(rlk, W8b):
+    """The bf16 saved-probabilities pair at full size: logp / lse bitwise, dH / dW within
+    the gradient tolerance of the recompute path (one extra bf16 rounding of p)."""
+    from gpu_util import rel_l2
+    w = workloads.QWEN3_8B
+    _, W = W8b
+    d = workloads.make_inputs(w, with_W=False)
+    h, y, g = dev_bf16(d["h"]), dev(d["y"]), dev(d["g"])
+    logp, lse = rlk.linear_logp_fwd(h, W, y, w.V_true)
+    dH, dW = rlk.linear_logp_bwd(h, W, y, lse, g, w.V_true, dH_fp32_partial=True)
+    (logp2, lse2), pbuf = rlk.linear_logp_fwd_save_probs(h, W, y, w.V_true)
+    assert torch.equal(logp, logp2) and torch.equal(lse, lse2)
+    dH2, dW2 = rlk.linear_logp_bwd_saved_probs(h, W, y, lse, g, pbuf, w.V_true, dH_fp32_partial=True)
+    eH = float((dH2 - dH).norm() / dH.norm())
+    eW = float((dW2 - dW).norm() / dW.norm())
+    assert eH <= 1e-2 and eW <= 1e-2, (eH, eW)
+    assert torch.all(dW2[w.V_true:] == 0)

@@ -233,3 +233,28 @@ def test_saved_logits_sharded_and_invalid_targets(rlk):
         assert torch.all(dHp[[5, 200]] == 0)
     torch.cuda.synchronize()
     assert int(err.item()) & rlk.RLK_FLAG_BAD_TARGET
+
+
+@pytest.mark.parametrize("T,H,V,Vt", [(300, 512, 20480, 20000), (129, 200, 2500, 2345), (64, 256, 4096, 4096)])
+def test_saved_probs_path(rlk, oracle_mod, T, H, V, Vt):
+    """bf16 saved probabilities: logp / lse bit-identical to the plain forward, gradients
+    within the tolerance of the oracle (not bitwise: p carries one bf16 rounding)."""
+    d = _inputs(T, H, V, Vt, seed=T * 3 + 2)
+    h, W, y, g = dev_bf16(d["h"]), dev_bf16(d["W"]), dev(d["y"]), dev(d["g"])
+    logp, lse = rlk.linear_logp_fwd(h, W, y, Vt)
+    (logp2, lse2), pbuf = rlk.linear_logp_fwd_save_probs(h, W, y, Vt)
+    assert torch.equal(logp, logp2) and torch.equal(lse, lse2)
+    dH, dW = rlk.linear_logp_bwd_saved_probs(h, W, y, lse, g, pbuf, Vt)
+    ref_lse = oracle_mod.forward(d["h"], d["W"], d["y"], Vt)[1]
+    g64 = d["g"].astype(np.float64)
+    ref_dH = oracle_mod.backward_dh(d["h"], d["W"], d["y"], g64, Vt)
+    ref_dW = oracle_mod.backward_dw(d["h"], d["W"], d["y"], g64, ref_lse, Vt)
+    assert_grad_close(host_bf16_to_f64(dH), ref_dH, what="dH (saved probs)")
+    assert_grad_close(dW.cpu().numpy(), ref_dW, what="dW (saved probs)")
+    assert torch.all(dW[Vt:] == 0)
+    # sharded: each shard's probabilities give its dW rows
+    for a, n in rlk.shard_bounds(V, Vt, 2) if V >= 20480 else []:
+        _, pb = rlk.linear_logp_fwd_save_probs(h, W[a:a + n], y, Vt, vocab_start=a, partial=True)
+        _, dWp = rlk.linear_logp_bwd_saved_probs(h, W[a:a + n], y, lse, g, pb, Vt, vocab_start=a,
+                                                 want_dH=False)
+        assert_grad_close(dWp.cpu().numpy(), ref_dW[a:a + n], what="shard dW (saved probs)")
