@@ -311,6 +311,36 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
   return r == CUDA_SUCCESS;
 }
 
+// MN-major operand [K rows][row_elems] (row_elems contiguous, the MN axis) whose tiles are
+// 128 wide in MN and 64 deep in K. With row_elems a multiple of 64 it is viewed as
+// {64 elements, K rows, row_elems / 64 atoms} with 3-D boxes {64, 64, 2}: one copy fetches
+// both 128-byte swizzle atoms of a tile, in the layout two 2-D 64 x 64 boxes give. Other
+// row lengths keep the 2-D map (the view's last atom would run past the row). *wide says
+// which one was made.
+bool encode_mn(CUtensorMap* m, const void* base, uint64_t row_elems, uint64_t k_rows, int32_t* wide) {
+  if (row_elems % 64 != 0) {
+    *wide = 0;
+    return encode_2d(m, base, row_elems, k_rows, row_elems, 64, 64);
+  }
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {64, k_rows, row_elems / 64};
+  cuuint64_t strides[2] = {row_elems * 2, 128};
+  cuuint32_t box[3] = {64, 64, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  *wide = 1;
+  return r == CUDA_SUCCESS;
+}
+
+// K-major token-row operand [T][row_elems] as the two A maps of TileMaps.
+bool encode_rows(TileMaps* m, const void* base, uint64_t row_elems, uint64_t T) {
+  return encode_2d(&m->a, base, row_elems, T, row_elems, 64, 64) &&
+         encode_2d(&m->a_full, base, row_elems, T, row_elems, 64, BM);
+}
+
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -455,9 +485,9 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
   float* ws = static_cast<float*>(workspace);  // [T][n_leaves_local][3] (fits in 3 * arr)
 
   if (g.n_leaves_local > 0) {
-    CUtensorMap tmA, tmB;
-    if (!encode_2d(&tmA, h, H, T, H, 64, 64)) return RLK_ERR_CUDA;  // 64-row boxes
-    if (!encode_2d(&tmB, W, H, V_local, H, 64, B_HALF)) return RLK_ERR_CUDA;
+    TileMaps maps;
+    if (!encode_rows(&maps, h, H, T)) return RLK_ERR_CUDA;
+    if (!encode_2d(&maps.b, W, H, V_local, H, 64, B_HALF)) return RLK_ERR_CUDA;
     GemmArgs a;
     a.T = static_cast<int32_t>(T);
     a.H = static_cast<int32_t>(H);
@@ -479,7 +509,7 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
     }
     a.err_flag = err_flag;
     a.stall_stage = stall_stage;
-    if (launch_gemm_fwd(tmA, tmB, a, s) != cudaSuccess) return RLK_ERR_CUDA;
+    if (launch_gemm_fwd(maps, a, s) != cudaSuccess) return RLK_ERR_CUDA;
   }
 
   TreeArgs ta;
@@ -617,9 +647,9 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
         err_flag);
     if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
   } else {
-    CUtensorMap tmA, tmB;
-    if (!encode_2d(&tmA, h, H, T, H, 64, 64)) return RLK_ERR_CUDA;  // 64-row boxes
-    if (!encode_2d(&tmB, W, H, V_local, H, 64, B_HALF)) return RLK_ERR_CUDA;
+    TileMaps maps;
+    if (!encode_rows(&maps, h, H, T)) return RLK_ERR_CUDA;
+    if (!encode_2d(&maps.b, W, H, V_local, H, 64, B_HALF)) return RLK_ERR_CUDA;
     GemmArgs a;
     a.T = static_cast<int32_t>(T);
     a.H = static_cast<int32_t>(H);
@@ -635,7 +665,7 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
     a.dz = dz;
     a.dz_ld = Vd;
     a.err_flag = err_flag;
-    if (launch_gemm_dz(tmA, tmB, a, s) != cudaSuccess) return RLK_ERR_CUDA;
+    if (launch_gemm_dz(maps, a, s) != cudaSuccess) return RLK_ERR_CUDA;
   }
 
   // 2. dH = dz W over this shard's valid columns
@@ -645,10 +675,10 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
     if (V_valid == 0) {
       if (cudaMemsetAsync(dH, 0, static_cast<size_t>(T) * H * elem, s) != cudaSuccess) return RLK_ERR_CUDA;
     } else {
-      CUtensorMap tmA, tmB;
-      if (!encode_2d(&tmA, dz, Vd, T, Vd, 64, 64)) return RLK_ERR_CUDA;  // 64-row boxes
-      if (!encode_2d(&tmB, W, H, V_local, H, 64, 64)) return RLK_ERR_CUDA;
+      TileMaps maps;
       GemmArgs a;
+      if (!encode_rows(&maps, dz, Vd, T)) return RLK_ERR_CUDA;
+      if (!encode_mn(&maps.b, W, H, V_local, &a.b_mn_wide)) return RLK_ERR_CUDA;
       a.T = static_cast<int32_t>(T);
       a.H = static_cast<int32_t>(H);
       a.n_mt = n_pm;
@@ -663,16 +693,17 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
       if (!dH_fp32_partial && a.n_kb > KC_BLOCKS)
         a.acc_scratch = reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_dz_bytes(T, V_local));
       a.err_flag = err_flag;
-      if (launch_gemm_dh(tmA, tmB, a, s) != cudaSuccess) return RLK_ERR_CUDA;
+      if (launch_gemm_dh(maps, a, s) != cudaSuccess) return RLK_ERR_CUDA;
     }
   }
 
   // 3. dW = dz^T h (rows at or above V_true come out exactly zero: their dz is zero)
   if (dW) {
-    CUtensorMap tmA, tmB;
-    if (!encode_2d(&tmA, dz, Vd, T, Vd, 64, 64)) return RLK_ERR_CUDA;
-    if (!encode_2d(&tmB, h, H, T, H, 64, 64)) return RLK_ERR_CUDA;
+    TileMaps maps;
     GemmArgs a;
+    if (!encode_mn(&maps.a, dz, Vd, T, &a.a_mn_wide)) return RLK_ERR_CUDA;
+    maps.a_full = maps.a;  // unused: dW's A is MN-major
+    if (!encode_mn(&maps.b, h, H, T, &a.b_mn_wide)) return RLK_ERR_CUDA;
     a.T = static_cast<int32_t>(T);
     a.H = static_cast<int32_t>(H);
     a.n_mt = static_cast<int32_t>(ceil_div(V_local, PAIR_M));
@@ -685,7 +716,7 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
     a.out_cols = static_cast<int32_t>(H);
     a.out_f32 = 1;
     a.err_flag = err_flag;
-    if (launch_gemm_dw(tmA, tmB, a, s) != cudaSuccess) return RLK_ERR_CUDA;
+    if (launch_gemm_dw(maps, a, s) != cudaSuccess) return RLK_ERR_CUDA;
   }
   return RLK_OK;
 }

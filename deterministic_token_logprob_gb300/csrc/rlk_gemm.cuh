@@ -127,8 +127,21 @@ __device__ __forceinline__ int a_boxes(int rows_left) {
   return rows_left <= 0 ? 0 : min(BM / A_BOX_ROWS, (rows_left + A_BOX_ROWS - 1) / A_BOX_ROWS);
 }
 
+// One 128(MN) x 64(K) MN-major tile: two 64 x 64 swizzle atoms at dst and dst + 8 KiB,
+// fetched by one copy of the 3-D view when `wide`, else by two 2-D copies. mn is a
+// multiple of 128.
+__device__ __forceinline__ void load_mn_tile(uint8_t* dst, const CUtensorMap* m, int32_t wide,
+                                             uint32_t bar, int mn, int k0, uint64_t pol) {
+  if (wide) {
+    tma_load_3d_pair(dst, m, bar, 0, k0, mn / 64, pol);
+  } else {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) tma_load_2d_pair(dst + q * MN_ATOM_BYTES, m, bar, mn + q * 64, k0, pol);
+  }
+}
+
 template <int MODE>
-__device__ void producer_loop(const CUtensorMap* tmA, const CUtensorMap* tmB, const GemmArgs& a,
+__device__ void producer_loop(const TileMaps& maps, const GemmArgs& a,
                               uint8_t* smem, uint64_t* full, uint64_t* empty, const PairCtx& c) {
   // L2 policy per operand: h is re-read by every leaf / vocab tile (fwd, dz) or by
   // every vocab tile of dW, so it is kept; the W tiles of fwd / dz are used by all
@@ -150,10 +163,11 @@ __device__ void producer_loop(const CUtensorMap* tmA, const CUtensorMap* tmB, co
       tile_origin<MODE>(a, item, j, m0, n0);
       const int am = m0 + r * BM;      // this CTA's A rows
       const int bn = n0 + r * B_HALF;  // this CTA's B rows
-      // Token-row A operands (fwd, dz, dH) load in 64-row boxes and skip boxes that lie
-      // wholly at or beyond T: accumulator rows are independent dot products, rows past T
-      // are never stored, and the zero fill would otherwise cost as much load bandwidth
-      // as real data (small batches).
+      // Token-row A operands (fwd, dz, dH) load as one 128-row box when all of this CTA's
+      // rows lie below T; otherwise in 64-row boxes, skipping those wholly at or beyond T:
+      // accumulator rows are independent dot products, rows past T are never stored, and
+      // the zero fill would otherwise cost as much load bandwidth as real data (small
+      // batches). The byte count is the same either way.
       const int boxes_mine = kAPerRow ? a_boxes(a.T - am) : 0;
       const int boxes_pair = kAPerRow ? a_boxes(a.T - m0) + a_boxes(a.T - m0 - BM) : 0;
       const uint32_t tx = kAPerRow ? static_cast<uint32_t>(boxes_pair * A_BOX_BYTES + PAIR * B_STAGE_BYTES)
@@ -174,22 +188,19 @@ __device__ void producer_loop(const CUtensorMap* tmA, const CUtensorMap* tmB, co
         }
         const int k0 = kb * BK;
         if constexpr (kAPerRow) {
-          for (int q = 0; q < boxes_mine; ++q)            // h / dz, K-major boxes 64 x 64
-            tma_load_2d_pair(sA + q * A_BOX_BYTES, tmA, bar, k0, am + q * A_BOX_ROWS, polA);
+          if (boxes_mine == BM / A_BOX_ROWS) {            // h / dz, K-major box 64 x 128
+            tma_load_2d_pair(sA, &maps.a_full, bar, k0, am, polA);
+          } else {
+            for (int q = 0; q < boxes_mine; ++q)          // ragged tail: boxes 64 x 64
+              tma_load_2d_pair(sA + q * A_BOX_BYTES, &maps.a, bar, k0, am + q * A_BOX_ROWS, polA);
+          }
+        } else {                                          // dz[k0.., am..], MN-major 128 x 64
+          load_mn_tile(sA, &maps.a, a.a_mn_wide, bar, am, k0, polA);
         }
         if constexpr (is_fwd<MODE> || MODE == MODE_DZ) {
-          tma_load_2d_pair(sB, tmB, bar, k0, bn, polB);   // W, K-major box 64 x 128
-        } else if constexpr (MODE == MODE_DH) {
-#pragma unroll
-          for (int q = 0; q < B_HALF / 64; ++q)           // W[k0.., bn+64q..], MN-major 64 x 64
-            tma_load_2d_pair(sB + q * MN_ATOM_BYTES, tmB, bar, bn + q * 64, k0, polB);
-        } else {
-#pragma unroll
-          for (int q = 0; q < BM / 64; ++q)               // dz[k0.., am+64q..], MN-major 64 x 64
-            tma_load_2d_pair(sA + q * MN_ATOM_BYTES, tmA, bar, am + q * 64, k0, polA);
-#pragma unroll
-          for (int q = 0; q < B_HALF / 64; ++q)           // h[k0.., bn+64q..], MN-major 64 x 64
-            tma_load_2d_pair(sB + q * MN_ATOM_BYTES, tmB, bar, bn + q * 64, k0, polB);
+          tma_load_2d_pair(sB, &maps.b, bar, k0, bn, polB);   // W, K-major box 64 x 128
+        } else {                                          // W (dH) / h (dW)[k0.., bn..], MN-major
+          load_mn_tile(sB, &maps.b, a.b_mn_wide, bar, bn, k0, polB);
         }
         ++issued;
       }
@@ -556,8 +567,7 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
 // ---------------------------------------------------------------------------
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const GemmArgs a) {
+    gemm_kernel(const __grid_constant__ TileMaps maps, const GemmArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -591,8 +601,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&maps.a);
+    if (MODE != MODE_DW) tma_prefetch_desc(&maps.a_full);
+    tma_prefetch_desc(&maps.b);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, TMEM_COLS);
@@ -605,7 +616,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) producer_loop<MODE>(&tmA, &tmB, a, smem, full, empty, c);
+    if (lane == 0) producer_loop<MODE>(maps, a, smem, full, empty, c);
   } else if (warp == 1) {
     if (lane == 0 && c.rank == 0)
       mma_loop<MODE>(a, smem, full, empty, acc_full, acc_empty, drain, tmem_base, c);
@@ -626,7 +637,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 template <int MODE>
-cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+cudaError_t launch_gemm(const TileMaps& maps, const GemmArgs& a,
                         cudaStream_t stream) {
   auto kernel = gemm_kernel<MODE>;
   cudaLaunchAttribute attr[1];
@@ -658,7 +669,7 @@ cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Ge
   }
   clusters = min(clusters, a.n_items);
   cfg.gridDim = dim3(PAIR * clusters, 1, 1);
-  e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, a);
+  e = cudaLaunchKernelEx(&cfg, kernel, maps, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -3,9 +3,9 @@
 
 namespace rlk {
 
-cudaError_t launch_gemm_dw(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+cudaError_t launch_gemm_dw(const TileMaps& maps, const GemmArgs& a,
                            cudaStream_t stream) {
-  return launch_gemm<MODE_DW>(tmA, tmB, a, stream);
+  return launch_gemm<MODE_DW>(maps, a, stream);
 }
 
 }  // namespace rlk

@@ -3,9 +3,9 @@
 
 namespace rlk {
 
-cudaError_t launch_gemm_dz(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+cudaError_t launch_gemm_dz(const TileMaps& maps, const GemmArgs& a,
                            cudaStream_t stream) {
-  return launch_gemm<MODE_DZ>(tmA, tmB, a, stream);
+  return launch_gemm<MODE_DZ>(maps, a, stream);
 }
 
 }  // namespace rlk

@@ -4,10 +4,10 @@
 
 namespace rlk {
 
-cudaError_t launch_gemm_fwd(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+cudaError_t launch_gemm_fwd(const TileMaps& maps, const GemmArgs& a,
                             cudaStream_t stream) {
-  if (a.p_out) return launch_gemm<MODE_FWDP>(tmA, tmB, a, stream);
-  return launch_gemm<MODE_FWD>(tmA, tmB, a, stream);
+  if (a.p_out) return launch_gemm<MODE_FWDP>(maps, a, stream);
+  return launch_gemm<MODE_FWD>(maps, a, stream);
 }
 
 }  // namespace rlk

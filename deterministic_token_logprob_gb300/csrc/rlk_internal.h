@@ -48,6 +48,19 @@ enum GemmMode : int {
   MODE_FWDP = 4, // MODE_FWD that also saves bf16 e(z - m) and the running maxima
 };
 
+// The tensor maps of one GEMM launch, passed as one __grid_constant__ parameter.
+//  a       K-major A (h or dz): 64-row boxes, for tiles whose rows run past T; MN-major A
+//          (dz of dW): see a_mn_wide
+//  a_full  K-major A: the same tensor in 128-row boxes, for tiles with all rows below T
+//  b       W or h: K-major 64 x 128 boxes (fwd, dz), or MN-major (dH, dW): see b_mn_wide
+// An MN-major operand is either a 2-D map with 64 x 64 boxes (two copies per 128-wide
+// tile) or, when its row length is a multiple of 64 elements, a 3-D view
+// {64 elements, K rows, row / 64 atoms} that fetches both 64-wide swizzle atoms of the
+// tile in one copy; the shared-memory image is the same.
+struct alignas(64) TileMaps {
+  CUtensorMap a, a_full, b;
+};
+
 struct GemmArgs {
   int32_t T = 0, H = 0;
   int32_t n_items = 0;
@@ -73,6 +86,7 @@ struct GemmArgs {
   int32_t out_rows = 0, out_cols = 0;
   int32_t out_f32 = 0;
   float* acc_scratch = nullptr;    // dH with bf16 output and several K chunks: fp32 running sum, ld = out_ld
+  int32_t a_mn_wide = 0, b_mn_wide = 0;  // MN-major maps are 3-D 128-wide views (TileMaps)
   int32_t n_mt = 0, n_nt = 0;      // dH / dW: 256-row pair tiles along M, 256-column tiles along N
   // Self-test only (rlk_selftest_wait_timeout): the even CTA arms its `stall_stage`-th
   // stage but issues none of its copies, so the wait on that stage cannot complete.
@@ -81,13 +95,13 @@ struct GemmArgs {
 
 // Launchers (one translation unit each): enqueue one cluster launch (pairs of CTAs,
 // as many pairs as can be resident, at most one per work item) on `stream`.
-cudaError_t launch_gemm_fwd(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+cudaError_t launch_gemm_fwd(const TileMaps& maps, const GemmArgs& a,
                             cudaStream_t stream);  // MODE_FWDP when a.p_out is set
-cudaError_t launch_gemm_dz(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+cudaError_t launch_gemm_dz(const TileMaps& maps, const GemmArgs& a,
                            cudaStream_t stream);
-cudaError_t launch_gemm_dh(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+cudaError_t launch_gemm_dh(const TileMaps& maps, const GemmArgs& a,
                            cudaStream_t stream);
-cudaError_t launch_gemm_dw(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+cudaError_t launch_gemm_dw(const TileMaps& maps, const GemmArgs& a,
                            cudaStream_t stream);
 
 }  // namespace rlk
