@@ -6,8 +6,11 @@ shares no code with it: the arithmetic lives in ``rlk_oracle.c`` (plain C99,
 binary64), compiled by :func:`build` with gcc.
 
 Inputs ``h`` and ``W`` are numpy arrays either of dtype float64 or of dtype
-uint16 holding raw bf16 bit patterns (the exact values the GPU receives). Each
-function states the definition it evaluates; the C file cites the passages.
+uint16 holding raw bf16 bit patterns (the exact values the GPU receives), or
+E4M3-quantized operands given as a pair ``(codes, scale)``: uint8 codes
+[rows, H] and one float64 scale per row, the value of an element being
+decode(code) * scale (see :func:`quantize_rows_e4m3`). Each function states the
+definition it evaluates; the C file cites the passages.
 """
 from __future__ import annotations
 
@@ -25,6 +28,11 @@ _LIB_PATH = os.path.join(_OUT_DIR, "librlk_oracle.so")
 
 F64 = 0
 BF16 = 1
+E4M3 = 2
+
+
+class _E4M3Rows(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scale", ctypes.c_void_p)]
 
 _lib = None
 _lock = threading.Lock()
@@ -57,11 +65,19 @@ def _load():
             lib.rlko_lse_merge.argtypes = [P, P, P, I64, I64, P, P]
             lib.rlko_backward_dh.argtypes = [I, P, P, P, P, I64, I64, I64, I64, P, I64, P, I]
             lib.rlko_backward_dw.argtypes = [I, P, P, P, P, P, I64, I64, I64, I64, P, I64, P, I]
+            lib.rlko_backward_dh_ste.argtypes = [I, P, P, I, P, P, P, P, I64, I64, I64, I64, P,
+                                                 I64, P, I]
+            lib.rlko_backward_dw_ste.argtypes = [I, P, P, I, P, P, P, P, I64, I64, I64, I64, P,
+                                                 I64, P, I]
+            lib.rlko_quantize_rows_e4m3.argtypes = [I, P, I64, I64, P, P]
+            lib.rlko_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            lib.rlko_e4m3_to_double.restype = ctypes.c_double
             lib.rlko_bf16_to_double.argtypes = [ctypes.c_uint16]
             lib.rlko_bf16_to_double.restype = ctypes.c_double
             lib.rlko_default_threads.argtypes = []
             for name in ("rlko_forward", "rlko_shard_stats", "rlko_lse_merge",
-                         "rlko_backward_dh", "rlko_backward_dw", "rlko_default_threads"):
+                         "rlko_backward_dh", "rlko_backward_dw", "rlko_default_threads",
+                         "rlko_backward_dh_ste", "rlko_backward_dw_ste", "rlko_quantize_rows_e4m3"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -76,26 +92,48 @@ def bf16_to_double(bits: int) -> float:
     return float(_load().rlko_bf16_to_double(int(bits) & 0xFFFF))
 
 
-def _mat(a: np.ndarray):
-    if a.dtype == np.float64:
-        return F64, np.ascontiguousarray(a)
-    if a.dtype == np.uint16:
-        return BF16, np.ascontiguousarray(a)
-    raise TypeError(f"oracle inputs must be float64 or uint16 (bf16 bits), got {a.dtype}")
+class _Operand:
+    """One matrix operand as the C side takes it: a kind code, a pointer, a shape.
+    Keeps the arrays (and, for E4M3, the descriptor struct) alive."""
+
+    def __init__(self, a):
+        if isinstance(a, tuple):
+            codes, scale = a
+            codes = np.ascontiguousarray(codes)
+            scale = np.ascontiguousarray(scale, dtype=np.float64)
+            if codes.dtype != np.uint8 or codes.ndim != 2 or scale.shape != (codes.shape[0],):
+                raise TypeError("E4M3 operands are (uint8 codes [rows, H], float64 scale [rows])")
+            self.kind, self.shape, self._keep = E4M3, codes.shape, (codes, scale)
+            self._desc = _E4M3Rows(codes.ctypes.data, scale.ctypes.data)
+            self.ptr = ctypes.cast(ctypes.pointer(self._desc), ctypes.c_void_p)
+            return
+        if a.dtype == np.float64:
+            self.kind = F64
+        elif a.dtype == np.uint16:
+            self.kind = BF16
+        else:
+            raise TypeError(f"oracle inputs must be float64, uint16 (bf16 bits) or (codes, scale), got {a.dtype}")
+        a = np.ascontiguousarray(a)
+        if a.ndim != 2:
+            raise ValueError("operands are 2-D")
+        self.shape, self._keep, self.ptr = a.shape, a, a.ctypes.data_as(ctypes.c_void_p)
 
 
-def _pair(h: np.ndarray, W: np.ndarray):
-    dh, h = _mat(h)
-    dw, W = _mat(W)
-    if dh != dw:
+def _pair(h, W):
+    oh, ow = _Operand(h), _Operand(W)
+    if oh.kind != ow.kind:
         raise TypeError("h and W must have the same element kind")
-    if h.ndim != 2 or W.ndim != 2 or h.shape[1] != W.shape[1]:
-        raise ValueError(f"shape mismatch h{h.shape} W{W.shape}")
-    return dh, h, W
+    if oh.shape[1] != ow.shape[1]:
+        raise ValueError(f"shape mismatch h{oh.shape} W{ow.shape}")
+    return oh.kind, oh, ow
 
 
 def _ptr(a):
-    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+    if a is None:
+        return None
+    if isinstance(a, _Operand):
+        return a.ptr
+    return a.ctypes.data_as(ctypes.c_void_p)
 
 
 def _rows(rows, T):
@@ -188,4 +226,67 @@ def backward_dw(h, W, y, g, lse, V_true, vrows=None, nthreads=0):
     _check(_load().rlko_backward_dw(kind, _ptr(h), _ptr(W), _ptr(y), _ptr(g), _ptr(lse), T, H, V,
                                     int(V_true), _ptr(r), n, _ptr(dW), int(nthreads)),
            "rlko_backward_dw")
+    return dW
+
+
+def e4m3_to_double(code: int) -> float:
+    """Value of one OCP E4M3 code (sign, 4 exponent bits with bias 7, 3 mantissa bits;
+    no infinities, S.1111.111 = NaN)."""
+    return float(_load().rlko_e4m3_to_double(int(code) & 0xFF))
+
+
+def quantize_rows_e4m3(x):
+    """Per-row power-of-two scale and E4M3 codes of x (float64, or uint16 bf16 bits):
+    e = the smallest integer with max|x_row| <= 448 * 2^e (0 for an all-zero row),
+    code = the E4M3 value nearest to x / 2^e, ties to the even code.
+    Returns (codes uint8 [rows, cols], scale float64 [rows] = 2^e)."""
+    o = _Operand(x)
+    if o.kind == E4M3:
+        raise TypeError("quantize_rows_e4m3 takes float64 or bf16 bits")
+    rows, cols = o.shape
+    q = np.empty((rows, cols), np.uint8)
+    scale = np.empty(rows, np.float64)
+    _check(_load().rlko_quantize_rows_e4m3(o.kind, o.ptr, rows, cols, _ptr(q), _ptr(scale)),
+           "rlko_quantize_rows_e4m3")
+    return q, scale
+
+
+def backward_dh_ste(zh, zW, h, W, y, g, V_true, rows=None, nthreads=0):
+    """Straight-through dH rows: p and dz from the logits of (zh, zW) (e.g. E4M3 operands),
+    dH_t = sum_v dz_tv W_v with the unquantized W."""
+    zk, zh, zW = _pair(zh, zW)
+    kind, h, W = _pair(h, W)
+    if zh.shape != h.shape or zW.shape != W.shape:
+        raise ValueError("logit and gradient operands must have the same shapes")
+    y = np.ascontiguousarray(y, dtype=np.int64)
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    T, H = h.shape
+    V = W.shape[0]
+    r, n = _rows(rows, T)
+    dH = np.empty((n, H), np.float64)
+    _check(_load().rlko_backward_dh_ste(zk, _ptr(zh), _ptr(zW), kind, _ptr(h), _ptr(W), _ptr(y),
+                                        _ptr(g), T, H, V, int(V_true), _ptr(r), n, _ptr(dH),
+                                        int(nthreads)), "rlko_backward_dh_ste")
+    return dH
+
+
+def backward_dw_ste(zh, zW, h, y, g, lse, V_true, vrows=None, nthreads=0):
+    """Straight-through dW rows: dz from the logits of (zh, zW) and the given lse,
+    dW_v = sum_t dz_tv h_t with the unquantized h; 0 for v >= V_true."""
+    zk, zh, zW = _pair(zh, zW)
+    oh = _Operand(h)
+    if zh.shape != oh.shape:
+        raise ValueError("logit and gradient operands must have the same shapes")
+    y = np.ascontiguousarray(y, dtype=np.int64)
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    lse = np.ascontiguousarray(lse, dtype=np.float64)
+    T, H = oh.shape
+    V = zW.shape[0]
+    if lse.shape != (T,):
+        raise ValueError("lse must have one entry per token")
+    r, n = _rows(vrows, V)
+    dW = np.empty((n, H), np.float64)
+    _check(_load().rlko_backward_dw_ste(zk, _ptr(zh), _ptr(zW), oh.kind, _ptr(oh), _ptr(y),
+                                        _ptr(g), _ptr(lse), T, H, V, int(V_true), _ptr(r), n,
+                                        _ptr(dW), int(nthreads)), "rlko_backward_dw_ste")
     return dW

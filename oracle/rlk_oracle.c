@@ -42,6 +42,28 @@
  * rounded values the GPU receives. All arithmetic is binary64. Targets outside
  * [0, V_true) give NaN log-probabilities and zero gradient rows.
  *
+ * FP8 LM head. The RL training forward may have to reproduce an FP8 inference
+ * GEMM: the weights are quantized to FP8 again at every forward, both sides use
+ * one quantization rounding rule and one batch-invariant GEMM for every batch
+ * size, and the backward takes gradients for the BF16 master weights with the
+ * quantization treated as the identity (straight-through estimator) (the AREX
+ * feed article on vLLM's bitwise-consistent RL training, sections
+ * "训练前向直接调用推理内核" -- the training forward calls the inference kernels --
+ * and "对齐的代价：逐算子拆解" -- the cost of alignment, operator by operator).
+ * The pages fix neither the FP8 format nor the scale granularity;
+ * the reading used here: OCP E4M3 ("FN": no infinities, max 448) with one
+ * power-of-two scale per row (per token of h, per vocab row of W), so that a
+ * token's quantized values never depend on the rest of the batch and the
+ * quantization is exactly reproducible:
+ *
+ *   e[r]     = the smallest integer with max_k |x[r][k]| <= 448 * 2^e   (0 for an all-zero row)
+ *   q[r][k]  = the E4M3 code nearest to x[r][k] / 2^e[r], ties to the even code
+ *   xq[r][k] = decode(q[r][k]) * 2^e[r]
+ *
+ * and the FP8 forward is the definition above evaluated on (hq, Wq); the STE
+ * backward forms p and dz from the logits of (hq, Wq) and contracts dz with the
+ * unquantized h and W.
+ *
  * Built with -O2 -ffp-contract=off and without -ffast-math (see build.py). The
  * dot product keeps four running sums; in binary64 the summation order changes
  * results only at the 1e-16 relative level, far below every tolerance in use.
@@ -55,6 +77,12 @@
 
 #define RLKO_F64 0
 #define RLKO_BF16 1
+#define RLKO_E4M3 2 /* operand = const rlko_e4m3_rows*: codes [rows][H] and a scale per row */
+
+typedef struct {
+  const uint8_t* codes;
+  const double* scale;
+} rlko_e4m3_rows;
 
 #define RLKO_OK 0
 #define RLKO_EINVAL 1
@@ -72,9 +100,88 @@ double rlko_bf16_to_double(uint16_t bits) {
   return (double)f;
 }
 
+/* OCP 8-bit floating point, E4M3: sign bit, 4 exponent bits (bias 7), 3 mantissa
+ * bits; exponent field 0 holds the subnormals M * 2^-9; S.1111.111 is NaN and there
+ * is no infinity, so the largest finite magnitude is 1.75 * 2^8 = 448. */
+double rlko_e4m3_to_double(uint8_t c) {
+  const int sign = c >> 7, E = (c >> 3) & 15, M = c & 7;
+  double v;
+  if (E == 15 && M == 7) return NAN;
+  if (E == 0)
+    v = ldexp((double)M, -9);
+  else
+    v = ldexp(1.0 + M / 8.0, E - 7);
+  return sign ? -v : v;
+}
+
+/* The E4M3 code nearest to y (|y| <= 448), ties to the code with the even mantissa.
+ * Positive codes 0 .. 126 are increasing in value, so a binary search finds the
+ * largest code not above |y|; its successor is the only other candidate. */
+static uint8_t e4m3_nearest(double y) {
+  const int neg = y < 0.0 || (y == 0.0 && signbit(y));
+  const double a = fabs(y);
+  int lo = 0, hi = 126;
+  while (lo < hi) { /* largest c with decode(c) <= a */
+    int mid = (lo + hi + 1) / 2;
+    if (rlko_e4m3_to_double((uint8_t)mid) <= a) lo = mid;
+    else hi = mid - 1;
+  }
+  int c = lo;
+  if (c < 126) {
+    const double d0 = a - rlko_e4m3_to_double((uint8_t)c);
+    const double d1 = rlko_e4m3_to_double((uint8_t)(c + 1)) - a;
+    if (d1 < d0 || (d1 == d0 && ((c + 1) & 1) == 0)) c = c + 1;
+  }
+  return (uint8_t)(neg ? (c | 0x80) : c);
+}
+
+/* Per-row power-of-two scale and E4M3 codes of x [rows][cols] (bf16 bits or
+ * float64, see the header comment for the definition). Non-finite inputs are
+ * outside the definition and rejected. */
+int rlko_quantize_rows_e4m3(int dtype, const void* x, int64_t rows, int64_t cols, uint8_t* q,
+                            double* scale) {
+  if (!x || !q || !scale || rows < 0 || cols < 0 || (dtype != RLKO_F64 && dtype != RLKO_BF16))
+    return RLKO_EINVAL;
+  double* buf = (double*)malloc(sizeof(double) * (size_t)(cols > 0 ? cols : 1));
+  if (!buf) return RLKO_ENOMEM;
+  for (int64_t r = 0; r < rows; ++r) {
+    double amax = 0.0;
+    if (dtype == RLKO_F64) {
+      memcpy(buf, (const double*)x + r * cols, (size_t)cols * sizeof(double));
+    } else {
+      const uint16_t* p = (const uint16_t*)x + r * cols;
+      for (int64_t k = 0; k < cols; ++k) buf[k] = rlko_bf16_to_double(p[k]);
+    }
+    for (int64_t k = 0; k < cols; ++k) {
+      if (!isfinite(buf[k])) {
+        free(buf);
+        return RLKO_EINVAL;
+      }
+      if (fabs(buf[k]) > amax) amax = fabs(buf[k]);
+    }
+    int e = 0;
+    if (amax > 0.0) {
+      int k2;
+      frexp(amax, &k2);      /* amax in [2^(k2-1), 2^k2) */
+      e = k2 - 9;            /* a first guess, then the two defining inequalities */
+      while (amax > ldexp(448.0, e)) ++e;
+      while (amax <= ldexp(448.0, e - 1)) --e;
+    }
+    scale[r] = ldexp(1.0, e);
+    for (int64_t k = 0; k < cols; ++k) q[r * cols + k] = e4m3_nearest(ldexp(buf[k], -e));
+  }
+  free(buf);
+  return RLKO_OK;
+}
+
 static void load_row(int dtype, const void* base, int64_t row, int64_t H, double* out) {
   if (dtype == RLKO_F64) {
     memcpy(out, (const double*)base + row * H, (size_t)H * sizeof(double));
+  } else if (dtype == RLKO_E4M3) {
+    const rlko_e4m3_rows* m = (const rlko_e4m3_rows*)base;
+    const uint8_t* p = m->codes + row * H;
+    const double s = m->scale[row];
+    for (int64_t k = 0; k < H; ++k) out[k] = rlko_e4m3_to_double(p[k]) * s;
   } else {
     const uint16_t* p = (const uint16_t*)base + row * H;
     for (int64_t k = 0; k < H; ++k) out[k] = rlko_bf16_to_double(p[k]);
@@ -158,9 +265,12 @@ static void parallel_for(int64_t n, int nthreads, range_fn fn, void* ctx) {
 /* ------------------------------------------------------------------------- */
 
 typedef struct {
-  int dtype;
+  int dtype;           /* h, W: the operands the gradients are contracted with */
   const void* h;
   const void* W;
+  int zdtype;          /* zh, zW: the operands the logits are formed from (the same */
+  const void* zh;      /* as h, W except in the straight-through FP8 backward)      */
+  const void* zW;
   const int64_t* y;
   const double* g;     /* backward only */
   const double* lse_in; /* dW only */
@@ -183,9 +293,9 @@ static int target_valid(int64_t y, int64_t V_true) { return y >= 0 && y < V_true
 static void logits_block(const job_ctx* c, int64_t i0, int64_t nb, int64_t v0, int64_t v1,
                          double* hbuf, double* wbuf, double* z) {
   const int64_t H = c->H, n = v1 - v0;
-  for (int64_t b = 0; b < nb; ++b) load_row(c->dtype, c->h, row_at(c, i0 + b), H, hbuf + b * H);
+  for (int64_t b = 0; b < nb; ++b) load_row(c->zdtype, c->zh, row_at(c, i0 + b), H, hbuf + b * H);
   for (int64_t v = v0; v < v1; ++v) {
-    load_row(c->dtype, c->W, v - c->vocab_start, H, wbuf);
+    load_row(c->zdtype, c->zW, v - c->vocab_start, H, wbuf);
     for (int64_t b = 0; b < nb; ++b) z[b * n + (v - v0)] = dot(hbuf + b * H, wbuf, H);
   }
 }
@@ -248,6 +358,7 @@ int rlko_forward(int dtype, const void* h, const void* W, const int64_t* y, int6
   job_ctx c;
   memset(&c, 0, sizeof c);
   c.dtype = dtype; c.h = h; c.W = W; c.y = y;
+  c.zdtype = dtype; c.zh = h; c.zW = W;
   c.T = T; c.H = H; c.V = V; c.V_true = V_true;
   c.vocab_start = 0; c.V_local = V;
   c.rows = rows; c.n_rows = n_rows;
@@ -318,6 +429,7 @@ int rlko_shard_stats(int dtype, const void* h, const void* W_local, const int64_
   job_ctx c;
   memset(&c, 0, sizeof c);
   c.dtype = dtype; c.h = h; c.W = W_local; c.y = y;
+  c.zdtype = dtype; c.zh = h; c.zW = W_local;
   c.T = T; c.H = H; c.V = V_local; c.V_true = V_true;
   c.vocab_start = vocab_start; c.V_local = V_local;
   c.rows = rows; c.n_rows = n_rows;
@@ -401,11 +513,17 @@ static void dh_range(void* vctx, int64_t begin, int64_t end, int tid) {
 /*
  * dH[i][:] for token rows[i] (every token when rows == NULL), of
  * L = sum_t g[t] * logp[t]. dH is [n_rows][H].
+ *
+ * The straight-through form takes the logits (hence p and dz) from the operands
+ * (zh, zW) and contracts dz with W: dH = dz W. With (zh, zW) = (h, W) it is the
+ * plain gradient.
  */
-int rlko_backward_dh(int dtype, const void* h, const void* W, const int64_t* y, const double* g,
-                     int64_t T, int64_t H, int64_t V, int64_t V_true, const int64_t* rows,
-                     int64_t n_rows, double* dH, int nthreads) {
-  if (!h || !W || !y || !g || !dH || T < 0 || H <= 0 || V_true < 1 || V_true > V) return RLKO_EINVAL;
+int rlko_backward_dh_ste(int zdtype, const void* zh, const void* zW, int dtype, const void* h,
+                         const void* W, const int64_t* y, const double* g, int64_t T, int64_t H,
+                         int64_t V, int64_t V_true, const int64_t* rows, int64_t n_rows, double* dH,
+                         int nthreads) {
+  if (!zh || !zW || !h || !W || !y || !g || !dH || T < 0 || H <= 0 || V_true < 1 || V_true > V)
+    return RLKO_EINVAL;
   if (!rows) n_rows = T;
   for (int64_t i = 0; rows && i < n_rows; ++i)
     if (rows[i] < 0 || rows[i] >= T) return RLKO_EINVAL;
@@ -413,6 +531,7 @@ int rlko_backward_dh(int dtype, const void* h, const void* W, const int64_t* y, 
   job_ctx c;
   memset(&c, 0, sizeof c);
   c.dtype = dtype; c.h = h; c.W = W; c.y = y; c.g = g;
+  c.zdtype = zdtype; c.zh = zh; c.zW = zW;
   c.T = T; c.H = H; c.V = V; c.V_true = V_true;
   c.vocab_start = 0; c.V_local = V;
   c.rows = rows; c.n_rows = n_rows;
@@ -422,10 +541,18 @@ int rlko_backward_dh(int dtype, const void* h, const void* W, const int64_t* y, 
   return c.failed ? RLKO_ENOMEM : RLKO_OK;
 }
 
+int rlko_backward_dh(int dtype, const void* h, const void* W, const int64_t* y, const double* g,
+                     int64_t T, int64_t H, int64_t V, int64_t V_true, const int64_t* rows,
+                     int64_t n_rows, double* dH, int nthreads) {
+  return rlko_backward_dh_ste(dtype, h, W, dtype, h, W, y, g, T, H, V, V_true, rows, n_rows, dH,
+                              nthreads);
+}
+
 /* dW rows: dW_v = sum_t dz[t][v] h_t, using the given per-token lse. */
 typedef struct {
   job_ctx* c;
-  const double* hwide; /* [T][H] widened hidden states */
+  const double* hwide;  /* [T][H] widened h (the gradient operand) */
+  const double* hzwide; /* [T][H] widened zh (the logit operand), or hwide */
 } dw_ctx;
 
 static void dw_range(void* vctx, int64_t begin, int64_t end, int tid) {
@@ -443,16 +570,15 @@ static void dw_range(void* vctx, int64_t begin, int64_t end, int tid) {
     double* out = c->out0 + i * H;
     memset(out, 0, sizeof(double) * (size_t)H);
     if (v >= c->V_true) continue; /* padded rows take no gradient */
-    load_row(c->dtype, c->W, v, H, wbuf);
+    load_row(c->zdtype, c->zW, v, H, wbuf); /* only the logits use W's row */
     for (int64_t t = 0; t < T; ++t) {
       double g = c->g[t];
       int64_t y = c->y[t];
       /* a zero upstream gradient or an invalid target contributes exactly nothing */
       if (g == 0.0 || !target_valid(y, c->V_true)) continue;
-      const double* ht = d->hwide + t * H;
-      double zv = dot(ht, wbuf, H);
+      double zv = dot(d->hzwide + t * H, wbuf, H);
       double dz = g * ((v == y ? 1.0 : 0.0) - exp(zv - c->lse_in[t]));
-      axpy(dz, ht, out, H);
+      axpy(dz, d->hwide + t * H, out, H);
     }
   }
   free(wbuf);
@@ -462,27 +588,50 @@ static void dw_range(void* vctx, int64_t begin, int64_t end, int tid) {
  * dW[i][:] for vocab row vrows[i] (every row of W when vrows == NULL, then
  * n_vrows must equal V), given lse[t] for every token with g[t] != 0 (tokens
  * with g[t] == 0 are skipped, so their lse entry is never read).
+ *
+ * The straight-through form takes the logits from (zh, zW) and contracts dz with
+ * h: dW = dz^T h. With (zh, zW) = (h, W) it is the plain gradient (W itself then
+ * enters only through the logits).
  */
-int rlko_backward_dw(int dtype, const void* h, const void* W, const int64_t* y, const double* g,
-                     const double* lse, int64_t T, int64_t H, int64_t V, int64_t V_true,
-                     const int64_t* vrows, int64_t n_vrows, double* dW, int nthreads) {
-  if (!h || !W || !y || !g || !lse || !dW || T < 0 || H <= 0 || V_true < 1 || V_true > V)
+int rlko_backward_dw_ste(int zdtype, const void* zh, const void* zW, int dtype, const void* h,
+                         const int64_t* y, const double* g, const double* lse, int64_t T,
+                         int64_t H, int64_t V, int64_t V_true, const int64_t* vrows,
+                         int64_t n_vrows, double* dW, int nthreads) {
+  if (!zh || !zW || !h || !y || !g || !lse || !dW || T < 0 || H <= 0 || V_true < 1 || V_true > V)
     return RLKO_EINVAL;
   if (!vrows) n_vrows = V;
   for (int64_t i = 0; vrows && i < n_vrows; ++i)
     if (vrows[i] < 0 || vrows[i] >= V) return RLKO_EINVAL;
-  double* hwide = (double*)malloc(sizeof(double) * (size_t)((T > 0 ? T : 1) * H));
-  if (!hwide) return RLKO_ENOMEM;
+  const size_t n = (size_t)((T > 0 ? T : 1) * H);
+  double* hwide = (double*)malloc(sizeof(double) * n);
+  double* hzwide = (zh == h && zdtype == dtype) ? hwide : (double*)malloc(sizeof(double) * n);
+  if (!hwide || !hzwide) {
+    free(hwide);
+    if (hzwide != hwide) free(hzwide);
+    return RLKO_ENOMEM;
+  }
   for (int64_t t = 0; t < T; ++t) load_row(dtype, h, t, H, hwide + t * H);
+  if (hzwide != hwide)
+    for (int64_t t = 0; t < T; ++t) load_row(zdtype, zh, t, H, hzwide + t * H);
   int nt = resolve_threads(nthreads);
   job_ctx c;
   memset(&c, 0, sizeof c);
-  c.dtype = dtype; c.h = h; c.W = W; c.y = y; c.g = g; c.lse_in = lse;
+  c.dtype = dtype; c.h = h; c.y = y; c.g = g; c.lse_in = lse;
+  c.zdtype = zdtype; c.zh = zh; c.zW = zW;
   c.T = T; c.H = H; c.V = V; c.V_true = V_true;
   c.rows = vrows; c.n_rows = n_vrows;
   c.out0 = dW;
-  dw_ctx d = {&c, hwide};
+  dw_ctx d = {&c, hwide, hzwide};
   parallel_for(n_vrows, nt, dw_range, &d);
+  if (hzwide != hwide) free(hzwide);
   free(hwide);
   return c.failed ? RLKO_ENOMEM : RLKO_OK;
+}
+
+int rlko_backward_dw(int dtype, const void* h, const void* W, const int64_t* y, const double* g,
+                     const double* lse, int64_t T, int64_t H, int64_t V, int64_t V_true,
+                     const int64_t* vrows, int64_t n_vrows, double* dW, int nthreads) {
+  if (!W) return RLKO_EINVAL;
+  return rlko_backward_dw_ste(dtype, h, W, dtype, h, y, g, lse, T, H, V, V_true, vrows, n_vrows,
+                              dW, nthreads);
 }
