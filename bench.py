@@ -369,6 +369,7 @@ def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int)
             line["saved_logits"] = saved_logits_leg(rlk, torch, path, wr, device, args, peak, peak_sus)
             line["saved_probs_bf16"] = saved_probs_leg(rlk, torch, path, wr, device, args, peak)
             line["small_T_forward"] = small_t_leg(rlk, torch, path, device, peaks)
+            line["fp8_e4m3"] = fp8_leg(rlk, torch, path, wr, device, args, peak)
         line["e2e"] = e2e(rlk, torch, path, wr, d, device, args)
         rate, cores, sample = oracle_sample_rate(wr, d)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
@@ -469,6 +470,97 @@ def saved_probs_leg(rlk, torch, path, w, device, args, peak):
             "saved_probs_bytes": rlk.saved_probs_bytes(w.T, w.V), "steps": K}
 
 
+def _time_calls(torch, device, fn, K, warmup=3):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(K):
+        fn()
+    b.record()
+    torch.cuda.synchronize(device)
+    return a.elapsed_time(b) / K
+
+
+def fp8_leg(rlk, torch, path, w, device, args, peak_bf16):
+    """The FP8 (E4M3, per-row power-of-two scales) LM head on the Qwen3-8B weight:
+    forward-only at T = 4096 with the weight codes resident (inference-style) and with
+    the weight re-quantized every call (training-style); the straight-through fwd+bwd
+    step at T = 8192 (quantize W and h, FP8 forward, FP8 dz recompute, bf16 dH / dW).
+    The FP8 GEMM rate is reported against 2x the measured bf16 burst (the nominal
+    dense fp8 : bf16 tensor ratio, 4.5 : 2.25 PFLOP/s)."""
+    peak8 = 2.0 * peak_bf16
+    K = max(args.steps, 10)
+    W = path.W
+    V, H = W.shape
+    Vt = w.V_true
+    Wq = torch.empty((V, H), dtype=torch.uint8, device=device)
+    Ws = torch.empty(V, dtype=torch.float32, device=device)
+    out = {"format": "OCP E4M3, one power-of-two scale per row", "peak_tflops_fp8": peak8,
+           "peak_source": "2 x measured bf16 burst (nominal dense fp8:bf16 ratio)"}
+
+    wf = workloads.QWEN3_8B_FWD
+    h4 = torch.from_numpy(workloads.make_h(wf.T, H, 0).view(np.int16)).view(torch.bfloat16).to(device)
+    y4 = torch.from_numpy(workloads.make_y(wf.T, Vt, 0)).to(device)
+    hq4 = torch.empty((wf.T, H), dtype=torch.uint8, device=device)
+    hs4 = torch.empty(wf.T, dtype=torch.float32, device=device)
+    lp4 = torch.empty(wf.T, dtype=torch.float32, device=device)
+    ls4 = torch.empty(wf.T, dtype=torch.float32, device=device)
+    ws4 = torch.empty(rlk.fwd_workspace_bytes(wf.T, H, V), dtype=torch.uint8, device=device)
+    rlk.quantize_rows_e4m3(W, out=(Wq, Ws))
+
+    def fwd_resident():
+        rlk.quantize_rows_e4m3(h4, out=(hq4, hs4))
+        rlk.linear_logp_fwd_fp8(hq4, hs4, Wq, Ws, y4, Vt, out=(lp4, ls4), workspace=ws4)
+
+    def fwd_gemm_only():
+        rlk.linear_logp_fwd_fp8(hq4, hs4, Wq, Ws, y4, Vt, out=(lp4, ls4), workspace=ws4)
+
+    def fwd_requant():
+        rlk.quantize_rows_e4m3(W, out=(Wq, Ws))
+        fwd_resident()
+
+    def quant_W():
+        rlk.quantize_rows_e4m3(W, out=(Wq, Ws))
+
+    flops4 = 2.0 * wf.T * H * Vt
+    ms_g = _time_calls(torch, device, fwd_gemm_only, K)
+    ms_r = _time_calls(torch, device, fwd_resident, K)
+    ms_q = _time_calls(torch, device, fwd_requant, K)
+    ms_w = _time_calls(torch, device, quant_W, K)
+    qbytes = V * H * 3 + V * 4     # read bf16 W, write codes and scales
+    out["forward_T4096"] = {
+        "workload": f"{wf.name} T={wf.T} H={H} V={V} V_true={Vt}",
+        "gemm_call_ms": ms_g, "gemm_tflops": flops4 / (ms_g / 1e3) / 1e12,
+        "gemm_frac_of_fp8_peak": flops4 / (ms_g / 1e3) / 1e12 / peak8,
+        "tokens_per_s_W_resident": wf.T / (ms_r / 1e3), "ms_W_resident": ms_r,
+        "tokens_per_s_W_requantized": wf.T / (ms_q / 1e3), "ms_W_requantized": ms_q}
+    out["quantize_W"] = {"ms": ms_w, "GBps": qbytes / (ms_w / 1e3) / 1e9}
+    del hq4, hs4, lp4, ls4, ws4
+
+    hq = torch.empty((w.T, H), dtype=torch.uint8, device=device)
+    hs = torch.empty(w.T, dtype=torch.float32, device=device)
+
+    def step():
+        rlk.quantize_rows_e4m3(W, out=(Wq, Ws))
+        rlk.quantize_rows_e4m3(path.h, out=(hq, hs))
+        rlk.linear_logp_fwd_fp8(hq, hs, Wq, Ws, path.y, Vt, out=(path.logp, path.lse),
+                                workspace=path.fws)
+        rlk.linear_logp_bwd_fp8(path.h, W, hq, hs, Wq, Ws, path.y, path.lse, path.g, Vt,
+                                out=(path.dH, path.dW), workspace=path.bws)
+
+    ms = _time_calls(torch, device, step, args.steps)
+    step_flops = 3.0 * 2.0 * w.T * H * Vt
+    out["ste_fwd_bwd_T8192"] = {
+        "tokens_per_s": w.T / (ms / 1e3), "ms_per_step": ms,
+        "frac_of_bf16_burst": step_flops / (peak_bf16 * 1e12) / (ms / 1e3),
+        "gpu_launches_per_step": 7, "steps": args.steps,
+        "note": "per step: quantize W and h, FP8 forward (2 kernels), FP8 dz + bf16 dH + bf16 dW"}
+    del Wq, Ws, hq, hs
+    return out
+
+
 def fwd_only(rlk, torch, W_bits, path, device, args, peak):
     """Forward-only tokens/s on the Qwen3-8B forward workload (T=4096), same W."""
     w = workloads.QWEN3_8B_FWD
@@ -548,6 +640,18 @@ def run_case(args):
     path.forward()
     if args.case == "fwd":
         call = path.forward
+    elif args.case in ("fwd8", "dz8"):
+        hq, hs = rlk.quantize_rows_e4m3(path.h)
+        Wq, Ws = rlk.quantize_rows_e4m3(path.W)
+        if args.case == "fwd8":
+            def call():
+                rlk.linear_logp_fwd_fp8(hq, hs, Wq, Ws, path.y, w.V_true, out=(path.logp, path.lse),
+                                        workspace=path.fws)
+        else:
+            def call():
+                rlk.linear_logp_bwd_fp8(path.h, path.W, hq, hs, Wq, Ws, path.y, path.lse, path.g,
+                                        w.V_true, out=(None, None), want_dH=False, want_dW=False,
+                                        workspace=path.bws)
     else:
         want_dH, want_dW = args.case == "dh", args.case == "dw"
 
@@ -566,10 +670,11 @@ def run_case(args):
         b.record()
         torch.cuda.synchronize(dev)
         ms.append(a.elapsed_time(b))
-    flops = 2.0 * w.T * w.H * w.V_true * (1 if args.case in ("fwd", "dz") else 2)
+    flops = 2.0 * w.T * w.H * w.V_true * (1 if args.case in ("fwd", "dz", "fwd8", "dz8") else 2)
     print(json.dumps({"case": args.case, "T": w.T, "H": w.H, "V": w.V, "V_true": w.V_true,
                       "ms": ms, "tflops_best": flops / (min(ms) / 1e3) / 1e12,
-                      "kernels_per_call": {"fwd": 2, "dz": 1, "dh": 2, "dw": 2}[args.case]}),
+                      "kernels_per_call": {"fwd": 2, "dz": 1, "dh": 2, "dw": 2, "fwd8": 2,
+                                           "dz8": 1}[args.case]}),
           flush=True)
 
 
@@ -581,7 +686,7 @@ def main():
     ap.add_argument("--impl", choices=["rlk", "reference"], default="rlk")
     ap.add_argument("--workload", choices=["qwen3_8b", "qwen3_30b_tp2", "tiny"], default="qwen3_8b")
     ap.add_argument("--quick", action="store_true", help="skip the forward-only, e2e and CPU legs")
-    ap.add_argument("--case", choices=["fwd", "dz", "dh", "dw"], default=None,
+    ap.add_argument("--case", choices=["fwd", "dz", "dh", "dw", "fwd8", "dz8"], default=None,
                     help="time one stage only (dz alone; dh / dw each after its dz)")
     ap.add_argument("--tokens", type=int, default=1024, help="tokens for --case")
     ap.add_argument("--vocab", type=int, default=0,

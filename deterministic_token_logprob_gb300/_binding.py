@@ -23,6 +23,7 @@ RLK_ERR_CUDA = 4
 
 RLK_FLAG_BAD_TARGET = 1
 RLK_FLAG_TIMEOUT = 2
+RLK_FLAG_NONFINITE = 4
 
 LEAF_WIDTH = 1024
 MAX_SHARDS = 8
@@ -85,6 +86,14 @@ def _load():
         lib.rlk_selftest_wait_timeout.restype = ctypes.c_int
         lib.rlk_shard_sum_bf16.argtypes = [P, I32, I64, P, P]
         lib.rlk_shard_sum_bf16.restype = ctypes.c_int
+        lib.rlk_quantize_rows_e4m3.argtypes = [P, I64, I64, P, P, P, P]
+        lib.rlk_quantize_rows_e4m3.restype = ctypes.c_int
+        lib.rlk_linear_logp_fwd_fp8.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, P, P, P, P,
+                                                P, SZ, P]
+        lib.rlk_linear_logp_fwd_fp8.restype = ctypes.c_int
+        lib.rlk_linear_logp_bwd_fp8.argtypes = [P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64,
+                                                P, I32, P, P, P, SZ, P]
+        lib.rlk_linear_logp_bwd_fp8.restype = ctypes.c_int
         lib.rlk_status_string.argtypes = [ctypes.c_int]
         lib.rlk_status_string.restype = ctypes.c_char_p
         lib.rlk_version.argtypes = []
@@ -463,3 +472,123 @@ def shard_bounds(V: int, V_true: int, S: int):
         b = V if i == S - 1 else min((i + 1) * per * width, V)
         out.append((a, b - a))
     return out
+
+
+# --------------------------------------------------------------------------- FP8 LM head
+
+
+def quantize_rows_e4m3(x: torch.Tensor, *, out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None,
+                       err_flag: Optional[torch.Tensor] = None, stream=None):
+    """rlk_quantize_rows_e4m3 -> (codes uint8 [rows, cols], scale fp32 [rows]).
+
+    scale[r] = 2^e with e the smallest integer such that max|x[r]| <= 448 * 2^e;
+    codes = E4M3(x / scale) rounded to nearest even.
+    """
+    _need(x, "x", torch.bfloat16, 2)
+    rows, cols = x.shape
+    if out is not None:
+        q, scale = out
+    else:
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+        scale = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _need(q, "q", torch.uint8, 2)
+    _need(scale, "scale", torch.float32, 1)
+    if tuple(q.shape) != (rows, cols) or scale.shape[0] != rows:
+        raise ValueError("shape mismatch")
+    if err_flag is not None:
+        _need(err_flag, "err_flag", torch.int32, 1)
+    st = _load().rlk_quantize_rows_e4m3(_ptr(x), rows, cols, _ptr(q), _ptr(scale), _ptr(err_flag),
+                                        _stream_handle(stream))
+    _check("rlk_quantize_rows_e4m3", st)
+    return q, scale
+
+
+def linear_logp_fwd_fp8(hq: torch.Tensor, h_scale: torch.Tensor, Wq: torch.Tensor,
+                        W_scale: torch.Tensor, y: torch.Tensor, V_true: int, *,
+                        vocab_start: int = 0, partial: bool = False,
+                        out: Optional[Sequence[torch.Tensor]] = None,
+                        err_flag: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None, stream=None):
+    """rlk_linear_logp_fwd_fp8 on E4M3 codes + per-row scales (from :func:`quantize_rows_e4m3`);
+    returns as :func:`linear_logp_fwd`."""
+    _need(hq, "hq", torch.uint8, 2)
+    _need(Wq, "Wq", torch.uint8, 2)
+    _need(h_scale, "h_scale", torch.float32, 1)
+    _need(W_scale, "W_scale", torch.float32, 1)
+    _need(y, "y", torch.int64, 1)
+    T, H = hq.shape
+    V_local = Wq.shape[0]
+    if Wq.shape[1] != H or y.shape[0] != T or h_scale.shape[0] != T or W_scale.shape[0] != V_local:
+        raise ValueError("shape mismatch")
+    dev = hq.device
+    ws = _workspace(fwd_workspace_bytes(T, H, V_local), dev, workspace)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    if partial:
+        p = out[0] if out is not None else torch.empty((T, 3), dtype=torch.float32, device=dev)
+        _need(p, "partial", torch.float32, 2)
+        logp = lse = None
+    else:
+        p = None
+        if out is not None:
+            logp, lse = out
+        else:
+            logp = torch.empty(T, dtype=torch.float32, device=dev)
+            lse = torch.empty(T, dtype=torch.float32, device=dev)
+        _need(logp, "logp", torch.float32, 1)
+        _need(lse, "lse", torch.float32, 1)
+    if err_flag is not None:
+        _need(err_flag, "err_flag", torch.int32, 1)
+    st = _load().rlk_linear_logp_fwd_fp8(_ptr(hq), _ptr(h_scale), _ptr(Wq), _ptr(W_scale), _ptr(y),
+                                         T, H, V_local, int(vocab_start), int(V_true), _ptr(logp),
+                                         _ptr(lse), _ptr(p), _ptr(err_flag), _ptr(ws), nbytes,
+                                         _stream_handle(stream))
+    _check("rlk_linear_logp_fwd_fp8", st)
+    return p if partial else (logp, lse)
+
+
+def linear_logp_bwd_fp8(h: torch.Tensor, W: torch.Tensor, hq: torch.Tensor, h_scale: torch.Tensor,
+                        Wq: torch.Tensor, W_scale: torch.Tensor, y: torch.Tensor, lse: torch.Tensor,
+                        g: torch.Tensor, V_true: int, *, vocab_start: int = 0,
+                        dH_fp32_partial: bool = False, want_dH: bool = True, want_dW: bool = True,
+                        out: Optional[Tuple[Optional[torch.Tensor], Optional[torch.Tensor]]] = None,
+                        err_flag: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None, stream=None):
+    """rlk_linear_logp_bwd_fp8 (straight-through): dz from the E4M3 logits, dH = dz W and
+    dW = dz^T h with the bf16 operands; returns (dH, dW) as :func:`linear_logp_bwd`."""
+    _need(h, "h", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 2)
+    _need(hq, "hq", torch.uint8, 2)
+    _need(Wq, "Wq", torch.uint8, 2)
+    _need(h_scale, "h_scale", torch.float32, 1)
+    _need(W_scale, "W_scale", torch.float32, 1)
+    _need(y, "y", torch.int64, 1)
+    _need(lse, "lse", torch.float32, 1)
+    _need(g, "g", torch.float32, 1)
+    T, H = h.shape
+    V_local = W.shape[0]
+    if (W.shape[1] != H or tuple(hq.shape) != (T, H) or tuple(Wq.shape) != (V_local, H)
+            or y.shape[0] != T or lse.shape[0] != T or g.shape[0] != T
+            or h_scale.shape[0] != T or W_scale.shape[0] != V_local):
+        raise ValueError("shape mismatch")
+    dev = h.device
+    if out is not None:
+        dH, dW = out
+    else:
+        dH = (torch.empty((T, H), dtype=torch.float32 if dH_fp32_partial else torch.bfloat16,
+                          device=dev) if want_dH else None)
+        dW = torch.empty((V_local, H), dtype=torch.float32, device=dev) if want_dW else None
+    if dH is not None:
+        _need(dH, "dH", torch.float32 if dH_fp32_partial else torch.bfloat16, 2)
+    if dW is not None:
+        _need(dW, "dW", torch.float32, 2)
+    if err_flag is not None:
+        _need(err_flag, "err_flag", torch.int32, 1)
+    ws = _workspace(bwd_workspace_bytes(T, H, V_local), dev, workspace)
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    st = _load().rlk_linear_logp_bwd_fp8(_ptr(h), _ptr(W), _ptr(hq), _ptr(h_scale), _ptr(Wq),
+                                         _ptr(W_scale), _ptr(y), _ptr(lse), _ptr(g), T, H, V_local,
+                                         int(vocab_start), int(V_true), _ptr(dH),
+                                         1 if dH_fp32_partial else 0, _ptr(dW), _ptr(err_flag),
+                                         _ptr(ws), nbytes, _stream_handle(stream))
+    _check("rlk_linear_logp_bwd_fp8", st)
+    return dH, dW

@@ -24,8 +24,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "librlk.so")
 
-SOURCES = ["rlk_api.cu", "rlk_gemm_fwd.cu", "rlk_gemm_dz.cu", "rlk_gemm_dh.cu", "rlk_gemm_dw.cu",
-           "rlk_noalloc.cu"]
+SOURCES = ["rlk_api.cu", "rlk_gemm_fwd.cu", "rlk_gemm_dz.cu", "rlk_gemm_dh.cu", "rlk_gemm_dw.cu", "rlk_gemm_fp8.cu",
+           "rlk_quant.cu", "rlk_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, f) for f in ("rlk_ptx.cuh", "rlk_gemm.cuh", "rlk_internal.h")] + [
     os.path.join(INCLUDE, "rlk.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -295,17 +295,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return g_encode;
 }
 
-// 2-D bf16 tensor [outer][inner] (inner contiguous), 128-byte swizzled boxes of
-// box_inner x box_outer elements; out-of-range elements read as zero.
+// 2-D tensor [outer][inner] (inner contiguous) of bf16 (elem_bytes 2) or E4M3 codes
+// (elem_bytes 1), 128-byte swizzled boxes of box_inner x box_outer elements;
+// out-of-range elements read as zero.
 bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_elems,
-               uint32_t box_inner, uint32_t box_outer) {
+               uint32_t box_inner, uint32_t box_outer, int elem_bytes = 2) {
   auto enc = encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {row_elems * 2};
+  cuuint64_t strides[1] = {row_elems * static_cast<uint64_t>(elem_bytes)};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+  const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box,
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -335,11 +337,19 @@ bool encode_mn(CUtensorMap* m, const void* base, uint64_t row_elems, uint64_t k_
   return r == CUDA_SUCCESS;
 }
 
-// K-major token-row operand [T][row_elems] as the two A maps of TileMaps.
-bool encode_rows(TileMaps* m, const void* base, uint64_t row_elems, uint64_t T) {
-  return encode_2d(&m->a, base, row_elems, T, row_elems, 64, 64) &&
-         encode_2d(&m->a_full, base, row_elems, T, row_elems, 64, BM);
+// K-major token-row operand [T][row_elems] as the two A maps of TileMaps (boxes of one
+// 128-byte swizzle atom along K: 64 bf16 or 128 E4M3 codes).
+bool encode_rows(TileMaps* m, const void* base, uint64_t row_elems, uint64_t T, int elem_bytes = 2) {
+  const uint32_t k_box = 128u / static_cast<uint32_t>(elem_bytes);
+  return encode_2d(&m->a, base, row_elems, T, row_elems, k_box, 64, elem_bytes) &&
+         encode_2d(&m->a_full, base, row_elems, T, row_elems, k_box, BM, elem_bytes);
 }
+
+// E4M3 operands of the FP8 entry points: codes in place of h / W plus their scales.
+struct Fp8In {
+  const float* h_scale;  // [T]
+  const float* W_scale;  // [V_local], 16-byte aligned
+};
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -462,9 +472,12 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
                     int64_t V_local, int64_t vocab_start, int64_t V_true, float* logp, float* lse,
                     rlk_lse_partial* partial, float* z_saved, size_t z_saved_bytes,
                     int32_t* err_flag, void* workspace, size_t workspace_bytes, void* stream,
-                    int32_t stall_stage = -1, void* p_saved = nullptr, size_t p_saved_bytes = 0) {
+                    int32_t stall_stage = -1, void* p_saved = nullptr, size_t p_saved_bytes = 0,
+                    const Fp8In* f8 = nullptr) {
   rlk_status st = common_checks(h, W, y, T, H, V_local, vocab_start, V_true);
   if (st != RLK_OK) return st;
+  if (f8 && (H % 16 != 0 || !f8->W_scale || !aligned16(f8->W_scale) || (T > 0 && !f8->h_scale)))
+    return RLK_ERR_INVALID_ARG;
   if (T > 0 && !partial && !logp && !lse) return RLK_ERR_INVALID_ARG;
   ShardGeom g;
   st = shard_geometry(V_local, vocab_start, V_true, &g);
@@ -485,9 +498,10 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
   float* ws = static_cast<float*>(workspace);  // [T][n_leaves_local][3] (fits in 3 * arr)
 
   if (g.n_leaves_local > 0) {
+    const int eb = f8 ? 1 : 2;  // element bytes of h / W
     TileMaps maps;
-    if (!encode_rows(&maps, h, H, T)) return RLK_ERR_CUDA;
-    if (!encode_2d(&maps.b, W, H, V_local, H, 64, B_HALF)) return RLK_ERR_CUDA;
+    if (!encode_rows(&maps, h, H, T, eb)) return RLK_ERR_CUDA;
+    if (!encode_2d(&maps.b, W, H, V_local, H, 128 / eb, B_HALF, eb)) return RLK_ERR_CUDA;
     GemmArgs a;
     a.T = static_cast<int32_t>(T);
     a.H = static_cast<int32_t>(H);
@@ -498,7 +512,11 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
     a.leaf0 = static_cast<int32_t>(g.leaf0);
     a.n_leaves = static_cast<int32_t>(g.n_leaves_local);
     a.n_items = a.n_pm * a.n_leaves;
-    a.n_kb = static_cast<int32_t>(ceil_div(H, BK));
+    a.n_kb = static_cast<int32_t>(ceil_div(H, f8 ? BK8 : BK));
+    if (f8) {
+      a.a_scale = f8->h_scale;
+      a.b_scale = f8->W_scale;
+    }
     a.y = y;
     a.ws = ws;
     a.z_out = z_saved;
@@ -509,7 +527,7 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
     }
     a.err_flag = err_flag;
     a.stall_stage = stall_stage;
-    if (launch_gemm_fwd(maps, a, s) != cudaSuccess) return RLK_ERR_CUDA;
+    if ((f8 ? launch_gemm_fwd8(maps, a, s) : launch_gemm_fwd(maps, a, s)) != cudaSuccess) return RLK_ERR_CUDA;
   }
 
   TreeArgs ta;
@@ -610,9 +628,16 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
                     const float* g, const float* z_saved, int64_t T, int64_t H, int64_t V_local,
                     int64_t vocab_start, int64_t V_true, void* dH, int32_t dH_fp32_partial,
                     float* dW, int32_t* err_flag, void* workspace, size_t workspace_bytes,
-                    void* stream, const void* p_saved = nullptr) {
+                    void* stream, const void* p_saved = nullptr, const void* hq = nullptr,
+                    const void* Wq = nullptr, const Fp8In* f8 = nullptr) {
   rlk_status st = common_checks(h, W, y, T, H, V_local, vocab_start, V_true);
   if (st != RLK_OK) return st;
+  if (f8) {  // straight-through: dz from the E4M3 logits, dH / dW with the bf16 operands
+    st = common_checks(hq, Wq, y, T, H, V_local, vocab_start, V_true);
+    if (st != RLK_OK) return st;
+    if (H % 16 != 0 || !f8->W_scale || !aligned16(f8->W_scale) || (T > 0 && !f8->h_scale))
+      return RLK_ERR_INVALID_ARG;
+  }
   if (T > 0 && (!lse || !g)) return RLK_ERR_INVALID_ARG;
   if ((dH && !aligned16(dH)) || (dW && !aligned16(dW))) return RLK_ERR_INVALID_ARG;
   if (T == 0) return RLK_OK;
@@ -647,9 +672,10 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
         err_flag);
     if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
   } else {
+    const int eb = f8 ? 1 : 2;  // element bytes of the logit operands
     TileMaps maps;
-    if (!encode_rows(&maps, h, H, T)) return RLK_ERR_CUDA;
-    if (!encode_2d(&maps.b, W, H, V_local, H, 64, B_HALF)) return RLK_ERR_CUDA;
+    if (!encode_rows(&maps, f8 ? hq : h, H, T, eb)) return RLK_ERR_CUDA;
+    if (!encode_2d(&maps.b, f8 ? Wq : W, H, V_local, H, 128 / eb, B_HALF, eb)) return RLK_ERR_CUDA;
     GemmArgs a;
     a.T = static_cast<int32_t>(T);
     a.H = static_cast<int32_t>(H);
@@ -658,14 +684,18 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
     a.V_true = static_cast<int32_t>(V_true);
     a.n_pm = n_pm;
     a.n_items = static_cast<int32_t>(Vd / BN) * n_pm;
-    a.n_kb = static_cast<int32_t>(ceil_div(H, BK));
+    a.n_kb = static_cast<int32_t>(ceil_div(H, f8 ? BK8 : BK));
+    if (f8) {
+      a.a_scale = f8->h_scale;
+      a.b_scale = f8->W_scale;
+    }
     a.y = y;
     a.lse = lse;
     a.g = g;
     a.dz = dz;
     a.dz_ld = Vd;
     a.err_flag = err_flag;
-    if (launch_gemm_dz(maps, a, s) != cudaSuccess) return RLK_ERR_CUDA;
+    if ((f8 ? launch_gemm_dz8(maps, a, s) : launch_gemm_dz(maps, a, s)) != cudaSuccess) return RLK_ERR_CUDA;
   }
 
   // 2. dH = dz W over this shard's valid columns
@@ -759,6 +789,28 @@ rlk_status rlk_linear_logp_bwd_saved_probs(const void* h, const void* W, const i
     return RLK_ERR_INVALID_ARG;
   return bwd_impl(h, W, y, lse, g, nullptr, T, H, V_local, vocab_start, V_true, dH,
                   dH_fp32_partial, dW, err_flag, workspace, workspace_bytes, stream, p_saved);
+}
+
+rlk_status rlk_linear_logp_fwd_fp8(const void* hq, const float* h_scale, const void* Wq,
+                                   const float* W_scale, const int64_t* y, int64_t T, int64_t H,
+                                   int64_t V_local, int64_t vocab_start, int64_t V_true, float* logp,
+                                   float* lse, rlk_lse_partial* partial, int32_t* err_flag,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  const Fp8In f8{h_scale, W_scale};
+  return fwd_impl(hq, Wq, y, T, H, V_local, vocab_start, V_true, logp, lse, partial, nullptr, 0,
+                  err_flag, workspace, workspace_bytes, stream, -1, nullptr, 0, &f8);
+}
+
+rlk_status rlk_linear_logp_bwd_fp8(const void* h, const void* W, const void* hq,
+                                   const float* h_scale, const void* Wq, const float* W_scale,
+                                   const int64_t* y, const float* lse, const float* g, int64_t T,
+                                   int64_t H, int64_t V_local, int64_t vocab_start, int64_t V_true,
+                                   void* dH, int32_t dH_fp32_partial, float* dW, int32_t* err_flag,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  const Fp8In f8{h_scale, W_scale};
+  return bwd_impl(h, W, y, lse, g, nullptr, T, H, V_local, vocab_start, V_true, dH,
+                  dH_fp32_partial, dW, err_flag, workspace, workspace_bytes, stream, nullptr, hq, Wq,
+                  &f8);
 }
 
 rlk_status rlk_shard_sum_bf16(const float* partials, int32_t S, int64_t n, void* out, void* stream) {

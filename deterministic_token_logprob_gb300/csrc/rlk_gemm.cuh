@@ -11,6 +11,12 @@
 //             (fourth reason: tiled logits / dlogits in a controlled workspace).
 //   MODE_DH   dH = dz W    (K = vocab, ascending), bf16 or fp32 output.
 //   MODE_DW   dW = dz^T h  (K = tokens, ascending), fp32 output.
+//   MODE_FWD8 / MODE_DZ8  MODE_FWD / MODE_DZ on E4M3 operands with one power-of-two
+//             scale per row: the accumulator of hq Wq^T is multiplied by
+//             h_scale[t] * W_scale[v] before the same epilogue (an FP8 LM head
+//             whose training forward re-quantizes its weights every step; AREX
+//             feed article on vLLM's bitwise-consistent RL training, section
+//             "对齐的代价：逐算子拆解").
 //
 // Kernel structure: clusters of two CTAs (one per SM, persistent) compute
 // 256 x 256 tiles with tcgen05 cta_group::2. Per CTA, 192 threads:
@@ -36,13 +42,19 @@
 namespace rlk {
 
 template <int MODE>
-constexpr bool is_fwd = (MODE == MODE_FWD || MODE == MODE_FWDP);
+constexpr bool is_fwd = (MODE == MODE_FWD || MODE == MODE_FWDP || MODE == MODE_FWD8);
+template <int MODE>
+constexpr bool is_dz = (MODE == MODE_DZ || MODE == MODE_DZ8);
+template <int MODE>
+constexpr bool is_e4m3 = (MODE == MODE_FWD8 || MODE == MODE_DZ8);
 
 template <int MODE>
 struct Operands {
   static constexpr bool A_MN = (MODE == MODE_DW);
   static constexpr bool B_MN = (MODE == MODE_DH || MODE == MODE_DW);
-  static constexpr uint32_t IDESC = make_idesc_bf16(PAIR_M, BN, A_MN, B_MN);
+  static constexpr uint32_t IDESC =
+      is_e4m3<MODE> ? make_idesc_e4m3(PAIR_M, BN) : make_idesc_bf16(PAIR_M, BN, A_MN, B_MN);
+  static constexpr int K_PER_STAGE = is_e4m3<MODE> ? BK8 : BK;  // K elements of one stage
 };
 
 // Number of 256-wide tiles in a work item.
@@ -73,7 +85,7 @@ __device__ __forceinline__ void tile_origin(const GemmArgs& a, int item, int j, 
     const int leaf_local = item / a.n_pm, pm = item % a.n_pm;
     m0 = pm * PAIR_M;
     n0 = (a.leaf0 + leaf_local) * LEAF + j * BN - a.vocab_start;
-  } else if constexpr (MODE == MODE_DZ) {
+  } else if constexpr (is_dz<MODE>) {
     const int vt = item / a.n_pm, pm = item % a.n_pm;
     m0 = pm * PAIR_M;
     n0 = vt * BN;
@@ -149,7 +161,7 @@ __device__ void producer_loop(const TileMaps& maps, const GemmArgs& a,
   const uint64_t pol_keep = policy_evict_last();
   const uint64_t pol_norm = policy_evict_normal();
   const uint64_t pol_first = policy_evict_first();
-  constexpr bool kZ = (is_fwd<MODE> || MODE == MODE_DZ);
+  constexpr bool kZ = (is_fwd<MODE> || is_dz<MODE>);
   constexpr bool kAPerRow = (MODE != MODE_DW);  // A rows are tokens (independent outputs)
   const uint64_t polA = kZ ? pol_keep : pol_norm;
   const uint64_t polB = (MODE == MODE_DW) ? pol_keep : (kZ ? pol_first : pol_norm);
@@ -186,7 +198,7 @@ __device__ void producer_loop(const TileMaps& maps, const GemmArgs& a,
           ++issued;  // self-test: this stage's bytes never arrive
           continue;
         }
-        const int k0 = kb * BK;
+        const int k0 = kb * Operands<MODE>::K_PER_STAGE;
         if constexpr (kAPerRow) {
           if (boxes_mine == BM / A_BOX_ROWS) {            // h / dz, K-major box 64 x 128
             tma_load_2d_pair(sA, &maps.a_full, bar, k0, am, polA);
@@ -197,8 +209,8 @@ __device__ void producer_loop(const TileMaps& maps, const GemmArgs& a,
         } else {                                          // dz[k0.., am..], MN-major 128 x 64
           load_mn_tile(sA, &maps.a, a.a_mn_wide, bar, am, k0, polA);
         }
-        if constexpr (is_fwd<MODE> || MODE == MODE_DZ) {
-          tma_load_2d_pair(sB, &maps.b, bar, k0, bn, polB);   // W, K-major box 64 x 128
+        if constexpr (kZ) {
+          tma_load_2d_pair(sB, &maps.b, bar, k0, bn, polB);   // W, K-major box 128 rows x 128 B
         } else {                                          // W (dH) / h (dW)[k0.., bn..], MN-major
           load_mn_tile(sB, &maps.b, a.b_mn_wide, bar, bn, k0, polB);
         }
@@ -263,7 +275,11 @@ __device__ void mma_loop(const GemmArgs& a, uint8_t* smem, uint64_t* full, uint6
                                         : make_smem_desc(a_base + k * 32, 16, 1024);
           const uint64_t bd = Ops::B_MN ? make_smem_desc(b_base + k * 2048, MN_ATOM_BYTES, 1024)
                                         : make_smem_desc(b_base + k * 32, 16, 1024);
-          umma_bf16_pair(d_tmem, ad, bd, Ops::IDESC, (kb != kb_begin || k != 0) ? 1u : 0u);
+          const uint32_t acc = (kb != kb_begin || k != 0) ? 1u : 0u;
+          if constexpr (is_e4m3<MODE>)
+            umma_e4m3_pair(d_tmem, ad, bd, Ops::IDESC, acc);
+          else
+            umma_bf16_pair(d_tmem, ad, bd, Ops::IDESC, acc);
         }
         umma_commit_pair_multicast(&empty[s], 0x3);  // stage s free in both CTAs
       }
@@ -375,6 +391,30 @@ __device__ __forceinline__ uint4 pack8_bf16(const float* v) {
   return w;
 }
 
+// E4M3 modes: z = acc * (s_row * s_col) for the 64 columns starting at local column
+// `col` (s_col = W_scale; columns at or beyond V_local take 0, their accumulator is 0).
+// Both scales are powers of two, so the products are exact while they stay normal.
+__device__ __forceinline__ void apply_row_col_scales(float (&v)[64], float s_row, const float* s_col,
+                                                     int col, int V_local) {
+  if (col + 64 <= V_local) {  // warp-uniform: every row of the warp shares the columns
+    const float4* p = reinterpret_cast<const float4*>(s_col + col);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const float4 c4 = __ldg(p + q);
+      v[4 * q] = __fmul_rn(v[4 * q], __fmul_rn(s_row, c4.x));
+      v[4 * q + 1] = __fmul_rn(v[4 * q + 1], __fmul_rn(s_row, c4.y));
+      v[4 * q + 2] = __fmul_rn(v[4 * q + 2], __fmul_rn(s_row, c4.z));
+      v[4 * q + 3] = __fmul_rn(v[4 * q + 3], __fmul_rn(s_row, c4.w));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      const float c1 = (col + i < V_local) ? __ldg(s_col + col + i) : 0.f;
+      v[i] = __fmul_rn(v[i], __fmul_rn(s_row, c1));
+    }
+  }
+}
+
 template <int MODE>
 __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* acc_empty,
                               uint32_t tmem_base, const PairCtx& c) {
@@ -398,9 +438,13 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
     float g_t = 0.f, nl = 0.f;
     bool yvalid = false;
     const int t = m0 + static_cast<int>(c.rank) * BM + row;  // token row (fwd, dz, dH) or vocab row (dW)
+    float s_row = 0.f;  // E4M3 modes: this token's scale
+    if constexpr (is_e4m3<MODE>) {
+      if (t < a.T) s_row = a.a_scale[t];
+    }
     if constexpr (is_fwd<MODE>) {
       if (t < a.T) yt = a.y[t];
-    } else if constexpr (MODE == MODE_DZ) {
+    } else if constexpr (is_dz<MODE>) {
       if (t < a.T) {
         yt = a.y[t];
         g_t = a.g[t];
@@ -432,6 +476,7 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
         for (int ch = 0; ch < BN; ch += 64) {
           float v[64];
           tmem_ld64(taddr + ch, v);
+          if constexpr (is_e4m3<MODE>) apply_row_col_scales(v, s_row, a.b_scale, static_cast<int>(lc) + ch, a.V_local);
           if (zrow) {  // saved logits: the accumulator exactly as computed
 #pragma unroll
             for (int q = 0; q < 16; ++q)
@@ -452,7 +497,7 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
             fwd_chunk(v, vcols - ch, tl - ch, st);
           }
         }
-      } else if constexpr (MODE == MODE_DZ) {
+      } else if constexpr (is_dz<MODE>) {
         const int gc0 = a.vocab_start + n0;
         const int vcols = max(0, min(min(BN, a.V_true - gc0), a.V_local - n0));
         const int tl = (yvalid && yt >= gc0 && yt < static_cast<int64_t>(gc0) + vcols)
@@ -463,6 +508,7 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
         for (int ch = 0; ch < BN; ch += 64) {
           float v[64];
           tmem_ld64(taddr + ch, v);
+          if constexpr (is_e4m3<MODE>) apply_row_col_scales(v, s_row, a.b_scale, n0 + ch, a.V_local);
           const int tli = tl - ch;
           float d_target = 0.f;
           const bool any_target = __any_sync(0xffffffffu, tli >= 0 && tli < 64);

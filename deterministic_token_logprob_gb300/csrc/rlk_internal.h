@@ -46,7 +46,14 @@ enum GemmMode : int {
   MODE_DH = 2,   // dH = dz W      (A K-major, B MN-major)
   MODE_DW = 3,   // dW = dz^T h    (A MN-major, B MN-major)
   MODE_FWDP = 4, // MODE_FWD that also saves bf16 e(z - m) and the running maxima
+  MODE_FWD8 = 5, // MODE_FWD on E4M3 operands: z = (hq Wq^T) * h_scale[t] * W_scale[v]
+  MODE_DZ8 = 6,  // MODE_DZ on E4M3 operands (the straight-through backward's logits)
 };
+
+// E4M3 modes: one 128-byte swizzle atom holds 128 K elements, so a stage spans
+// BK8 = 128 of K (the same bytes as BK bf16 elements); one tcgen05.mma kind::f8f6f4
+// takes K = 32 (the same 32-byte step through the atom as K = 16 of bf16).
+constexpr int BK8 = 128;
 
 // The tensor maps of one GEMM launch, passed as one __grid_constant__ parameter.
 //  a       K-major A (h or dz): 64-row boxes, for tiles whose rows run past T; MN-major A
@@ -87,6 +94,9 @@ struct GemmArgs {
   int32_t out_f32 = 0;
   float* acc_scratch = nullptr;    // dH with bf16 output and several K chunks: fp32 running sum, ld = out_ld
   int32_t a_mn_wide = 0, b_mn_wide = 0;  // MN-major maps are 3-D 128-wide views (TileMaps)
+  // E4M3 modes: per-token scale of hq [T] and per-local-row scale of Wq [V_local]
+  const float* a_scale = nullptr;
+  const float* b_scale = nullptr;
   int32_t n_mt = 0, n_nt = 0;      // dH / dW: 256-row pair tiles along M, 256-column tiles along N
   // Self-test only (rlk_selftest_wait_timeout): the even CTA arms its `stall_stage`-th
   // stage but issues none of its copies, so the wait on that stage cannot complete.
@@ -101,6 +111,8 @@ cudaError_t launch_gemm_dz(const TileMaps& maps, const GemmArgs& a,
                            cudaStream_t stream);
 cudaError_t launch_gemm_dh(const TileMaps& maps, const GemmArgs& a,
                            cudaStream_t stream);
+cudaError_t launch_gemm_fwd8(const TileMaps& maps, const GemmArgs& a, cudaStream_t stream);
+cudaError_t launch_gemm_dz8(const TileMaps& maps, const GemmArgs& a, cudaStream_t stream);
 cudaError_t launch_gemm_dw(const TileMaps& maps, const GemmArgs& a,
                            cudaStream_t stream);
 

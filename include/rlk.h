@@ -90,6 +90,7 @@ typedef enum {
 /* bits ORed into *err_flag by the kernels */
 #define RLK_FLAG_BAD_TARGET 1
 #define RLK_FLAG_TIMEOUT 2
+#define RLK_FLAG_NONFINITE 4 /* rlk_quantize_rows_e4m3: a row held a NaN or an infinity */
 
 /* tiling constants that are part of the numerical contract */
 #define RLK_LEAF_WIDTH 1024
@@ -261,6 +262,68 @@ RLK_API rlk_status rlk_linear_logp_bwd_saved_probs(const void* h, const void* W,
  */
 RLK_API rlk_status rlk_shard_sum_bf16(const float* partials, int32_t S, int64_t n, void* out,
                               void* stream);
+
+/*
+ * FP8 LM head. An RL trainer whose rollouts run an FP8 output layer reproduces it
+ * in the training forward: the weights are quantized to FP8 again at every
+ * forward, both sides use one quantization rounding rule and one batch-invariant
+ * GEMM for every batch size, and the backward takes gradients for the bf16 master
+ * weights with the quantization treated as the identity (straight-through
+ * estimator) (AREX feed article on vLLM's bitwise-consistent RL training, sections
+ * "训练前向直接调用推理内核" and "对齐的代价：逐算子拆解"). The pages fix neither the
+ * FP8 format nor the scale granularity; this library uses OCP E4M3 (no infinities,
+ * largest magnitude 448) with one power-of-two scale per row, so a token's codes
+ * never depend on the rest of the batch and quantization is exactly reproducible.
+ *
+ * rlk_quantize_rows_e4m3: for each row r of x (bf16 [rows][cols], device, 16-byte
+ * aligned, cols % 8 == 0):
+ *   e       = the smallest integer with max_k |x[r][k]| <= 448 * 2^e (0 if the row is all zero)
+ *   scale[r] = 2^e                                   (fp32 [rows], device)
+ *   q[r][k]  = E4M3 code nearest to x[r][k] / 2^e, ties to even (uint8 [rows][cols], device,
+ *             16-byte aligned)
+ * A row holding a NaN or an infinity gets scale NaN and zero codes, and
+ * RLK_FLAG_NONFINITE is ORed into *err_flag (device int32, or NULL). rows == 0 or
+ * cols == 0 launches nothing. Asynchronous on `stream`; argument errors are returned
+ * before any launch.
+ */
+RLK_API rlk_status rlk_quantize_rows_e4m3(const void* x, int64_t rows, int64_t cols, void* q,
+                                          float* scale, int32_t* err_flag, void* stream);
+
+/*
+ * FP8 forward: the forward of rlk_linear_logp_fwd on E4M3 operands,
+ *   z[t][v] = (sum_k hq[t][k] * Wq[v][k]) * h_scale[t] * W_scale[v]
+ * (products exact, fp32 tensor-core accumulation over K in ascending 128-element
+ * steps, then the two power-of-two scales), with the same fixed merge tree, shard
+ * statistics, masking, outputs and errors.
+ *   hq       E4M3 codes [T][H] (device, 16-byte aligned), h_scale fp32 [T]
+ *   Wq       E4M3 codes [V_local][H] (device, 16-byte aligned), W_scale fp32 [V_local]
+ *            (device, 16-byte aligned)
+ * as produced by rlk_quantize_rows_e4m3; H % 16 == 0. Workspace: as
+ * rlk_linear_logp_fwd_workspace(T, H, V_local).
+ */
+RLK_API rlk_status rlk_linear_logp_fwd_fp8(const void* hq, const float* h_scale, const void* Wq,
+                                           const float* W_scale, const int64_t* y, int64_t T,
+                                           int64_t H, int64_t V_local, int64_t vocab_start,
+                                           int64_t V_true, float* logp, float* lse,
+                                           rlk_lse_partial* partial, int32_t* err_flag,
+                                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Straight-through FP8 backward: dz[t][v] = g[t] (1[v = y[t]] - e(z[t][v] - lse[t]))
+ * with z the E4M3 logits of rlk_linear_logp_fwd_fp8 (recomputed tile by tile, the
+ * same bits as that forward's), then dH = dz W and dW = dz^T h with the bf16
+ * operands h, W exactly as in rlk_linear_logp_bwd (outputs, shard partials, workspace
+ * rlk_linear_logp_bwd_workspace(T, H, V_local), errors). hq, h_scale, Wq, W_scale as
+ * in rlk_linear_logp_fwd_fp8; lse is the FP8 forward's.
+ */
+RLK_API rlk_status rlk_linear_logp_bwd_fp8(const void* h, const void* W, const void* hq,
+                                           const float* h_scale, const void* Wq,
+                                           const float* W_scale, const int64_t* y,
+                                           const float* lse, const float* g, int64_t T, int64_t H,
+                                           int64_t V_local, int64_t vocab_start, int64_t V_true,
+                                           void* dH, int32_t dH_fp32_partial, float* dW,
+                                           int32_t* err_flag, void* workspace,
+                                           size_t workspace_bytes, void* stream);
 
 /*
  * Forward without a workspace argument, for callers that cannot allocate device

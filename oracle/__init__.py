@@ -69,7 +69,7 @@ def _load():
                                                  I64, P, I]
             lib.rlko_backward_dw_ste.argtypes = [I, P, P, I, P, P, P, P, I64, I64, I64, I64, P,
                                                  I64, P, I]
-            lib.rlko_quantize_rows_e4m3.argtypes = [I, P, I64, I64, P, P]
+            lib.rlko_quantize_rows_e4m3.argtypes = [I, P, I64, I64, P, P, I]
             lib.rlko_e4m3_to_double.argtypes = [ctypes.c_uint8]
             lib.rlko_e4m3_to_double.restype = ctypes.c_double
             lib.rlko_bf16_to_double.argtypes = [ctypes.c_uint16]
@@ -235,7 +235,7 @@ def e4m3_to_double(code: int) -> float:
     return float(_load().rlko_e4m3_to_double(int(code) & 0xFF))
 
 
-def quantize_rows_e4m3(x):
+def quantize_rows_e4m3(x, nthreads=0):
     """Per-row power-of-two scale and E4M3 codes of x (float64, or uint16 bf16 bits):
     e = the smallest integer with max|x_row| <= 448 * 2^e (0 for an all-zero row),
     code = the E4M3 value nearest to x / 2^e, ties to the even code.
@@ -246,8 +246,8 @@ def quantize_rows_e4m3(x):
     rows, cols = o.shape
     q = np.empty((rows, cols), np.uint8)
     scale = np.empty(rows, np.float64)
-    _check(_load().rlko_quantize_rows_e4m3(o.kind, o.ptr, rows, cols, _ptr(q), _ptr(scale)),
-           "rlko_quantize_rows_e4m3")
+    _check(_load().rlko_quantize_rows_e4m3(o.kind, o.ptr, rows, cols, _ptr(q), _ptr(scale),
+                                           int(nthreads)), "rlko_quantize_rows_e4m3")
     return q, scale
 
 

@@ -114,64 +114,11 @@ double rlko_e4m3_to_double(uint8_t c) {
   return sign ? -v : v;
 }
 
-/* The E4M3 code nearest to y (|y| <= 448), ties to the code with the even mantissa.
- * Positive codes 0 .. 126 are increasing in value, so a binary search finds the
- * largest code not above |y|; its successor is the only other candidate. */
-static uint8_t e4m3_nearest(double y) {
-  const int neg = y < 0.0 || (y == 0.0 && signbit(y));
-  const double a = fabs(y);
-  int lo = 0, hi = 126;
-  while (lo < hi) { /* largest c with decode(c) <= a */
-    int mid = (lo + hi + 1) / 2;
-    if (rlko_e4m3_to_double((uint8_t)mid) <= a) lo = mid;
-    else hi = mid - 1;
-  }
-  int c = lo;
-  if (c < 126) {
-    const double d0 = a - rlko_e4m3_to_double((uint8_t)c);
-    const double d1 = rlko_e4m3_to_double((uint8_t)(c + 1)) - a;
-    if (d1 < d0 || (d1 == d0 && ((c + 1) & 1) == 0)) c = c + 1;
-  }
-  return (uint8_t)(neg ? (c | 0x80) : c);
-}
-
-/* Per-row power-of-two scale and E4M3 codes of x [rows][cols] (bf16 bits or
- * float64, see the header comment for the definition). Non-finite inputs are
- * outside the definition and rejected. */
-int rlko_quantize_rows_e4m3(int dtype, const void* x, int64_t rows, int64_t cols, uint8_t* q,
-                            double* scale) {
-  if (!x || !q || !scale || rows < 0 || cols < 0 || (dtype != RLKO_F64 && dtype != RLKO_BF16))
-    return RLKO_EINVAL;
-  double* buf = (double*)malloc(sizeof(double) * (size_t)(cols > 0 ? cols : 1));
-  if (!buf) return RLKO_ENOMEM;
-  for (int64_t r = 0; r < rows; ++r) {
-    double amax = 0.0;
-    if (dtype == RLKO_F64) {
-      memcpy(buf, (const double*)x + r * cols, (size_t)cols * sizeof(double));
-    } else {
-      const uint16_t* p = (const uint16_t*)x + r * cols;
-      for (int64_t k = 0; k < cols; ++k) buf[k] = rlko_bf16_to_double(p[k]);
-    }
-    for (int64_t k = 0; k < cols; ++k) {
-      if (!isfinite(buf[k])) {
-        free(buf);
-        return RLKO_EINVAL;
-      }
-      if (fabs(buf[k]) > amax) amax = fabs(buf[k]);
-    }
-    int e = 0;
-    if (amax > 0.0) {
-      int k2;
-      frexp(amax, &k2);      /* amax in [2^(k2-1), 2^k2) */
-      e = k2 - 9;            /* a first guess, then the two defining inequalities */
-      while (amax > ldexp(448.0, e)) ++e;
-      while (amax <= ldexp(448.0, e - 1)) --e;
-    }
-    scale[r] = ldexp(1.0, e);
-    for (int64_t k = 0; k < cols; ++k) q[r * cols + k] = e4m3_nearest(ldexp(buf[k], -e));
-  }
-  free(buf);
-  return RLKO_OK;
+/* rlko_e4m3_to_double of every code, filled once */
+static double g_e4m3_value[256];
+static pthread_once_t g_e4m3_once = PTHREAD_ONCE_INIT;
+static void e4m3_table_init(void) {
+  for (int c = 0; c < 256; ++c) g_e4m3_value[c] = rlko_e4m3_to_double((uint8_t)c);
 }
 
 static void load_row(int dtype, const void* base, int64_t row, int64_t H, double* out) {
@@ -181,7 +128,8 @@ static void load_row(int dtype, const void* base, int64_t row, int64_t H, double
     const rlko_e4m3_rows* m = (const rlko_e4m3_rows*)base;
     const uint8_t* p = m->codes + row * H;
     const double s = m->scale[row];
-    for (int64_t k = 0; k < H; ++k) out[k] = rlko_e4m3_to_double(p[k]) * s;
+    pthread_once(&g_e4m3_once, e4m3_table_init);
+    for (int64_t k = 0; k < H; ++k) out[k] = g_e4m3_value[p[k]] * s;
   } else {
     const uint16_t* p = (const uint16_t*)base + row * H;
     for (int64_t k = 0; k < H; ++k) out[k] = rlko_bf16_to_double(p[k]);
@@ -258,6 +206,88 @@ static void parallel_for(int64_t n, int nthreads, range_fn fn, void* ctx) {
   free(started);
   free(jobs);
   free(th);
+}
+
+/* The E4M3 code nearest to y (|y| <= 448), ties to the code with the even mantissa.
+ * Positive codes 0 .. 126 are increasing in value (tab[c] = their values), so a
+ * binary search finds the largest code not above |y|; its successor is the only
+ * other candidate. */
+static uint8_t e4m3_nearest(double y, const double* tab) {
+  const int neg = y < 0.0 || (y == 0.0 && signbit(y));
+  const double a = fabs(y);
+  int lo = 0, hi = 126;
+  while (lo < hi) { /* largest c with tab[c] <= a */
+    int mid = (lo + hi + 1) / 2;
+    if (tab[mid] <= a) lo = mid;
+    else hi = mid - 1;
+  }
+  int c = lo;
+  if (c < 126) {
+    const double d0 = a - tab[c];
+    const double d1 = tab[c + 1] - a;
+    if (d1 < d0 || (d1 == d0 && ((c + 1) & 1) == 0)) c = c + 1;
+  }
+  return (uint8_t)(neg ? (c | 0x80) : c);
+}
+
+typedef struct {
+  int dtype;
+  const void* x;
+  int64_t cols;
+  uint8_t* q;
+  double* scale;
+  double tab[127];
+  int failed; /* 1: out of memory, 2: a non-finite input */
+} quant_ctx;
+
+static void quantize_range(void* vctx, int64_t begin, int64_t end, int tid) {
+  quant_ctx* c = (quant_ctx*)vctx;
+  (void)tid;
+  const int64_t cols = c->cols;
+  double* buf = (double*)malloc(sizeof(double) * (size_t)(cols > 0 ? cols : 1));
+  if (!buf) {
+    c->failed = 1;
+    return;
+  }
+  for (int64_t r = begin; r < end; ++r) {
+    double amax = 0.0;
+    load_row(c->dtype, c->x, r, cols, buf);
+    for (int64_t k = 0; k < cols; ++k) {
+      if (!isfinite(buf[k])) {
+        c->failed = 2;
+        free(buf);
+        return;
+      }
+      if (fabs(buf[k]) > amax) amax = fabs(buf[k]);
+    }
+    int e = 0;
+    if (amax > 0.0) {
+      int k2;
+      frexp(amax, &k2); /* amax in [2^(k2-1), 2^k2) */
+      e = k2 - 9;       /* a first guess, then the two defining inequalities */
+      while (amax > ldexp(448.0, e)) ++e;
+      while (amax <= ldexp(448.0, e - 1)) --e;
+    }
+    c->scale[r] = ldexp(1.0, e);
+    for (int64_t k = 0; k < cols; ++k) c->q[r * cols + k] = e4m3_nearest(ldexp(buf[k], -e), c->tab);
+  }
+  free(buf);
+}
+
+/* Per-row power-of-two scale and E4M3 codes of x [rows][cols] (bf16 bits or
+ * float64, see the header comment for the definition), rows split over threads.
+ * Non-finite inputs are outside the definition and rejected. */
+int rlko_quantize_rows_e4m3(int dtype, const void* x, int64_t rows, int64_t cols, uint8_t* q,
+                            double* scale, int nthreads) {
+  if (!x || !q || !scale || rows < 0 || cols < 0 || (dtype != RLKO_F64 && dtype != RLKO_BF16))
+    return RLKO_EINVAL;
+  quant_ctx c;
+  memset(&c, 0, sizeof c);
+  c.dtype = dtype; c.x = x; c.cols = cols; c.q = q; c.scale = scale;
+  for (int i = 0; i < 127; ++i) c.tab[i] = rlko_e4m3_to_double((uint8_t)i);
+  parallel_for(rows, resolve_threads(nthreads), quantize_range, &c);
+  if (c.failed == 2) return RLKO_EINVAL;
+  return c.failed ? RLKO_ENOMEM : RLKO_OK;
 }
 
 /* ------------------------------------------------------------------------- */

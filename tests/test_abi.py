@@ -178,3 +178,48 @@ def test_saved_probs_queries_and_errors(lib):
     rest = (4, 64, 4096, 0, 4096, FAKE, 0, FAKE, None, FAKE, 1 << 30, None)
     assert lib.rlk_linear_logp_bwd_saved_probs(*bargs, None, need, *rest) == INVALID
     assert lib.rlk_linear_logp_bwd_saved_probs(*bargs, FAKE, need - 1, *rest) == INVALID
+
+
+def test_fp8_argument_errors(lib):
+    # quantizer
+    assert lib.rlk_quantize_rows_e4m3(FAKE, 0, 64, FAKE, FAKE, None, None) == OK
+    assert lib.rlk_quantize_rows_e4m3(None, 0, 0, None, None, None, None) == OK
+    assert lib.rlk_quantize_rows_e4m3(FAKE, -1, 64, FAKE, FAKE, None, None) == INVALID
+    assert lib.rlk_quantize_rows_e4m3(FAKE, 4, 60, FAKE, FAKE, None, None) == INVALID  # cols % 8
+    assert lib.rlk_quantize_rows_e4m3(MISALIGNED, 4, 64, FAKE, FAKE, None, None) == INVALID
+    assert lib.rlk_quantize_rows_e4m3(FAKE, 4, 64, FAKE, None, None, None) == INVALID
+    # forward: hq, h_scale, Wq, W_scale, y, T, H, V_local, vocab_start, V_true, logp, lse, partial,
+    #          err, ws, ws_bytes, stream
+    ws = lib.rlk_linear_logp_fwd_workspace(4, 64, 4096)
+
+    def f8(**k):
+        a = dict(hq=FAKE, hs=FAKE, Wq=FAKE, Ws=FAKE, y=FAKE, T=4, H=64, V=4096, vs=0, Vt=4096,
+                 logp=FAKE, lse=FAKE, part=None, err=None, ws=FAKE, nb=ws, s=None)
+        a.update(k)
+        return lib.rlk_linear_logp_fwd_fp8(*a.values())
+
+    assert f8(T=0) == OK
+    assert f8(H=72) == INVALID                 # H % 16 != 0 (E4M3 rows need 16-byte strides)
+    assert f8(hs=None) == INVALID
+    assert f8(Ws=None) == INVALID
+    assert f8(Ws=ctypes.c_void_p(0x100004)) == INVALID   # W_scale not 16-byte aligned
+    assert f8(Wq=MISALIGNED) == INVALID
+    assert f8(nb=ws - 1) == WORKSPACE
+    assert f8(T=0, hq=None, hs=None, y=None) == OK
+    # backward: h, W, hq, h_scale, Wq, W_scale, y, lse, g, T, H, V_local, vocab_start, V_true,
+    #           dH, partial, dW, err, ws, ws_bytes, stream
+    bws = lib.rlk_linear_logp_bwd_workspace(4, 64, 4096)
+
+    def b8(**k):
+        a = dict(h=FAKE, W=FAKE, hq=FAKE, hs=FAKE, Wq=FAKE, Ws=FAKE, y=FAKE, lse=FAKE, g=FAKE, T=4,
+                 H=64, V=4096, vs=0, Vt=4096, dH=FAKE, part=0, dW=FAKE, err=None, ws=FAKE, nb=bws,
+                 s=None)
+        a.update(k)
+        return lib.rlk_linear_logp_bwd_fp8(*a.values())
+
+    assert b8(T=0) == OK
+    assert b8(Wq=None) == INVALID
+    assert b8(hq=MISALIGNED) == INVALID
+    assert b8(H=72) == INVALID
+    assert b8(Ws=None) == INVALID
+    assert b8(nb=bws - 1) == WORKSPACE
