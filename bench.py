@@ -333,6 +333,7 @@ def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int)
     total_ms = t_start.elapsed_time(t_end)
     fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
     bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
+    step_ms = sorted(a.elapsed_time(c) for a, _, c in ev)
     total_ms = max_over_ranks(total_ms, world, device)
     ms_per_step = total_ms / K
     tokens_per_s = job_tokens_per_s(w.T, world, K, total_ms)
@@ -359,7 +360,8 @@ def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int)
         "step_roofline": {"flops_counted": step_flops, "roofline_ms": roofline_ms,
                           "frac_of_burst": roofline_ms / ms_per_step,
                           "frac_of_sustained": (step_flops / (peak_sus * 1e12) * 1e3) / ms_per_step,
-                          "fwd_ms": fwd_avg, "bwd_ms": statistics.mean(bwd_ms)},
+                          "fwd_ms": fwd_avg, "bwd_ms": statistics.mean(bwd_ms),
+                          "step_ms_median": statistics.median(step_ms), "step_ms_best": step_ms[0]},
         "clocks": clocks,
     }
 
