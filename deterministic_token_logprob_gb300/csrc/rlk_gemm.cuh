@@ -57,11 +57,29 @@ struct Operands {
   static constexpr int K_PER_STAGE = is_e4m3<MODE> ? BK8 : BK;  // K elements of one stage
 };
 
+// Work-item order of the forward and dz kernels: items are (vocab unit, token pair-tile)
+// pairs, vocab unit = leaf (forward) or 256-column tile (dz). Token pair-tiles are taken in
+// groups of TOKEN_GROUP; inside a group the items run vocab-unit-major. The clusters
+// working at one time then share a few W units and at most TOKEN_GROUP token tiles of h
+// (32 MiB of bf16 h at H = 4096), which stay in L2 while W streams past; with all token
+// tiles in flight (T = 8192: 64 MiB) h was re-fetched from DRAM for nearly every leaf.
+// The order changes only which cluster computes a tile and when, never a tile's arithmetic.
+constexpr int TOKEN_GROUP = 16;
+
+__device__ __forceinline__ void item_unit_pm(const GemmArgs& a, int n_units, int item, int& unit, int& pm) {
+  const int g0 = (item / (TOKEN_GROUP * n_units)) * TOKEN_GROUP;  // first token tile of the group
+  const int gsize = min(TOKEN_GROUP, a.n_pm - g0);
+  const int r = item - g0 * n_units;
+  unit = r / gsize;
+  pm = g0 + r % gsize;
+}
+
 // Number of 256-wide tiles in a work item.
 template <int MODE>
 __device__ __forceinline__ int item_tiles(const GemmArgs& a, int item) {
   if constexpr (is_fwd<MODE>) {
-    const int leaf_local = item / a.n_pm;
+    int leaf_local, pm;
+    item_unit_pm(a, a.n_leaves, item, leaf_local, pm);
     const int col0 = (a.leaf0 + leaf_local) * LEAF;
     const int end = min(col0 + LEAF, a.V_true);
     return (end - col0 + BN - 1) / BN;
@@ -82,11 +100,13 @@ __device__ __forceinline__ int tile_chunks(const GemmArgs& a) {
 template <int MODE>
 __device__ __forceinline__ void tile_origin(const GemmArgs& a, int item, int j, int& m0, int& n0) {
   if constexpr (is_fwd<MODE>) {
-    const int leaf_local = item / a.n_pm, pm = item % a.n_pm;
+    int leaf_local, pm;
+    item_unit_pm(a, a.n_leaves, item, leaf_local, pm);
     m0 = pm * PAIR_M;
     n0 = (a.leaf0 + leaf_local) * LEAF + j * BN - a.vocab_start;
   } else if constexpr (is_dz<MODE>) {
-    const int vt = item / a.n_pm, pm = item % a.n_pm;
+    int vt, pm;
+    item_unit_pm(a, a.n_items / a.n_pm, item, vt, pm);
     m0 = pm * PAIR_M;
     n0 = vt * BN;
   } else {
@@ -598,7 +618,8 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
 
     if constexpr (is_fwd<MODE>) {
       if (ok && t < a.T) {
-        const int leaf_local = item / a.n_pm;
+        int leaf_local, pm;
+        item_unit_pm(a, a.n_leaves, item, leaf_local, pm);
         float* o = a.ws + (static_cast<size_t>(t) * a.n_leaves + leaf_local) * 3;
         o[0] = st.m;
         o[1] = st.s;
