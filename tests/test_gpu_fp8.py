@@ -191,3 +191,76 @@ def test_qwen3_8b_fp8_full_size_sampled(rlk, oracle_mod):
                          | {w.V_true, w.V - 1}), dtype=np.int64)
     ref_dW = oracle_mod.backward_dw_ste(ohq, oWq, d["h"], d["y"], g64, lse_full, w.V_true, vrows=vr)
     assert_grad_close(dW.cpu().numpy()[vr], ref_dW, what="dW rows")
+
+
+def test_fp8_batch_invariance_full(rlk, oracle_mod):
+    """128 fixed targets inside ragged batches T in {1, 7, 128, 1000, 4097} at the Qwen3-8B
+    shape, FP8 path: each batch is quantized on the GPU (per-row scales, so a target's codes
+    never depend on its batch); logp, lse and straight-through dH rows bitwise equal across T."""
+    H, V, Vt = 4096, 151936, 151669
+    W_bits = workloads.make_W(V, H, 0)
+    W = dev_bf16(W_bits)
+    Wq, Ws = rlk.quantize_rows_e4m3(W)
+    th, ty = workloads.invariance_targets(0, H=H, V_true=Vt)
+    n = th.shape[0]
+    g_target = np.linspace(-1.0, 1.0, n).astype(np.float32)
+    seen = {}
+    for T in workloads.INVARIANCE_T:
+        logp_t = np.full(n, np.nan, np.float32)
+        lse_t = np.full(n, np.nan, np.float32)
+        dH_t = np.zeros((n, H), np.float32)
+        for b in workloads.invariance_batches(T, 0, H=H, V_true=Vt):
+            g = np.random.default_rng(T).standard_normal(T).astype(np.float32)
+            g[b.target_rows] = g_target[b.target_ids]
+            hd, yd, gd = dev_bf16(b.h), dev(b.y), dev(g)
+            hq, hs = rlk.quantize_rows_e4m3(hd)
+            logp, lse = rlk.linear_logp_fwd_fp8(hq, hs, Wq, Ws, yd, Vt)
+            dH, _ = rlk.linear_logp_bwd_fp8(hd, W, hq, hs, Wq, Ws, yd, lse, gd, Vt, want_dW=False,
+                                            dH_fp32_partial=True)
+            logp_t[b.target_ids] = logp.cpu().numpy()[b.target_rows]
+            lse_t[b.target_ids] = lse.cpu().numpy()[b.target_rows]
+            dH_t[b.target_ids] = dH.cpu().numpy()[b.target_rows]
+        assert not np.isnan(logp_t).any()
+        seen[T] = (logp_t, lse_t, dH_t)
+    T0 = workloads.INVARIANCE_T[0]
+    for T in workloads.INVARIANCE_T[1:]:
+        for a, b in zip(seen[T], seen[T0]):
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), T
+    pick = np.arange(0, n, 16)
+    ohq = oracle_mod.quantize_rows_e4m3(th[pick])
+    oWq = oracle_mod.quantize_rows_e4m3(W_bits)
+    ref_logp, _ = oracle_mod.forward(ohq, oWq, ty[pick], Vt)
+    assert_logp_close(seen[T0][0][pick], ref_logp)
+
+
+def test_qwen3_30b_tp2_fp8_sharded(rlk, oracle_mod):
+    """The 30B shape (T = 16384, H = 2048) in its two vocab shards on the FP8 path: merged
+    shard statistics bitwise equal to the unsharded FP8 forward; sampled tokens against the
+    oracle; sharded straight-through dH (fp32 partials, fixed-order sum) against the unsharded."""
+    w = workloads.QWEN3_30B_TP2
+    W_bits = workloads.make_W(w.V, w.H, 0)
+    W = dev_bf16(W_bits)
+    d = workloads.make_inputs(w, with_W=False)
+    h, y = dev_bf16(d["h"]), dev(d["y"])
+    hq, hs = rlk.quantize_rows_e4m3(h)
+    Wq, Ws = rlk.quantize_rows_e4m3(W)
+    logp, lse = rlk.linear_logp_fwd_fp8(hq, hs, Wq, Ws, y, w.V_true)
+    parts = torch.stack([rlk.linear_logp_fwd_fp8(hq, hs, Wq[a:a + n], Ws[a:a + n], y, w.V_true,
+                                                 vocab_start=a, partial=True)
+                         for a, n in w.shards])
+    slogp, slse = rlk.lse_merge(parts)
+    assert torch.equal(slogp, logp) and torch.equal(slse, lse)
+    rows = workloads.sample_rows(w.T, 12, seed=14)
+    ref_logp, _ = oracle_mod.forward(oracle_mod.quantize_rows_e4m3(d["h"][rows]),
+                                     oracle_mod.quantize_rows_e4m3(W_bits), d["y"][rows], w.V_true)
+    assert_logp_close(slogp.cpu().numpy()[rows], ref_logp)
+    g = dev(d["g"])
+    dH_full, _ = rlk.linear_logp_bwd_fp8(h, W, hq, hs, Wq, Ws, y, lse, g, w.V_true, want_dW=False)
+    dH_parts = torch.stack([
+        rlk.linear_logp_bwd_fp8(h, W[a:a + n], hq, hs, Wq[a:a + n], Ws[a:a + n], y, slse, g,
+                                w.V_true, vocab_start=a, dH_fp32_partial=True, want_dW=False)[0]
+        for a, n in w.shards])
+    dH = rlk.shard_sum_bf16(dH_parts)
+    from gpu_util import rel_l2
+    e = rel_l2(host_bf16_to_f64(dH), host_bf16_to_f64(dH_full))
+    assert e <= 1e-2, e
