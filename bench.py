@@ -127,16 +127,21 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- oracle timing
 
 
-def oracle_sample_rate(w: workloads.Workload, d: dict, n_tok: int = 16, n_vrows: int = 1024,
+def oracle_sample_rate(w: workloads.Workload, d: dict, n_tok: int = 0, n_vrows: int = 1024,
                        seed: int = 0):
     """Oracle (fp64, all host cores) fwd+bwd throughput on a bounded sample.
 
-    n_tok sampled tokens go through the oracle's forward and dH; dW is
-    evaluated for n_vrows sampled vocab rows (with g restricted to the sampled
-    tokens) and its time scaled by V / n_vrows. Returns (tokens/s, cores, sample text).
+    n_tok sampled tokens (default 8 per host thread, the oracle's own block of tokens per
+    thread) go through the oracle's forward and dH. dW is linear in the tokens with
+    non-zero g, so it is evaluated with g restricted to the sampled tokens for n_vrows
+    sampled vocab rows; its per-row time is scaled to all V rows, and its fixed cost
+    (widening h once per call) is charged per token (n_tok / T of it), as in a full step.
+    Returns (tokens/s, cores, sample text).
     """
     import oracle
     oracle.build()
+    cores = oracle.default_threads()
+    n_tok = min(w.T, n_tok or 8 * cores)
     rows = workloads.sample_rows(w.T, n_tok, seed=seed, stream=11)
     vrows = workloads.sample_rows(w.V, n_vrows, seed=seed, stream=12)
     g_sub = np.zeros(w.T, np.float64)
@@ -148,12 +153,18 @@ def oracle_sample_rate(w: workloads.Workload, d: dict, n_tok: int = 16, n_vrows:
     t2 = time.perf_counter()
     lse_full = np.zeros(w.T)
     lse_full[rows] = lse_rows
-    oracle.backward_dw(d["h"], d["W"], d["y"], g_sub, lse_full, w.V_true, vrows=vrows)
+    oracle.backward_dw(d["h"], d["W"], d["y"], g_sub, lse_full, w.V_true,
+                       vrows=np.zeros(0, np.int64))
     t3 = time.perf_counter()
-    per_step = (t1 - t0) + (t2 - t1) + (t3 - t2) * (w.V / len(vrows))
+    oracle.backward_dw(d["h"], d["W"], d["y"], g_sub, lse_full, w.V_true, vrows=vrows)
+    t4 = time.perf_counter()
+    fixed = t3 - t2
+    per_row = max(0.0, (t4 - t3) - fixed) / len(vrows)
+    per_step = (t1 - t0) + (t2 - t1) + per_row * w.V + fixed * len(rows) / w.T
     sample = (f"{len(rows)} of {w.T} tokens: oracle forward + dH over all {w.V_true} columns; "
-              f"dW for {len(vrows)} of {w.V} vocab rows, time scaled by {w.V / len(vrows):.1f}")
-    return len(rows) / per_step, oracle.default_threads(), sample
+              f"dW for {len(vrows)} of {w.V} vocab rows (per-row time x {w.V}), "
+              f"its fixed per-call cost charged {len(rows)}/{w.T}")
+    return len(rows) / per_step, cores, sample
 
 
 def run_reference(args, w: workloads.Workload, rank: int, world: int):
@@ -161,9 +172,11 @@ def run_reference(args, w: workloads.Workload, rank: int, world: int):
     if rank != 0:
         return
     d = workloads.make_inputs(w)
-    n_tok = 4 if w.T >= 4096 else min(w.T, 16)
+    import oracle
+    oracle.build()
+    n_tok = min(w.T, 2 * oracle.default_threads())   # a bounded sample per step (a few seconds)
     for i in range(args.warmup):
-        oracle_sample_rate(w, d, n_tok=n_tok, n_vrows=256, seed=100 + i)
+        oracle_sample_rate(w, d, n_tok=min(n_tok, 4), n_vrows=64, seed=100 + i)
     rates = []
     t0 = time.perf_counter()
     for i in range(args.steps):
