@@ -36,6 +36,8 @@
 // instruction sequence regardless of T, batch composition or SM count.
 #pragma once
 
+#include <atomic>
+
 #include "rlk_internal.h"
 #include "rlk_ptx.cuh"
 
@@ -721,11 +723,11 @@ cudaError_t launch_gemm(const TileMaps& maps, const GemmArgs& a,
   cfg.numAttrs = 1;
   // Shared-memory opt-in and resident pairs of this kernel, once per device (both
   // are properties of the device; racing first calls compute the same values).
-  static int resident[64] = {};
+  static std::atomic<int> resident[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int clusters = dev < 64 ? resident[dev] : 0;
+  int clusters = (dev >= 0 && dev < 64) ? resident[dev].load(std::memory_order_relaxed) : 0;
   if (clusters <= 0) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -733,7 +735,7 @@ cudaError_t launch_gemm(const TileMaps& maps, const GemmArgs& a,
     e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
     if (e != cudaSuccess) return e;
     if (clusters <= 0) return cudaErrorInvalidConfiguration;
-    if (dev < 64) resident[dev] = clusters;
+    if (dev >= 0 && dev < 64) resident[dev].store(clusters, std::memory_order_relaxed);
   }
   clusters = min(clusters, a.n_items);
   cfg.gridDim = dim3(PAIR * clusters, 1, 1);
