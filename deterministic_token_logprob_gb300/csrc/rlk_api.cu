@@ -511,6 +511,7 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
     a.n_pm = static_cast<int32_t>(ceil_div(T, PAIR_M));
     a.leaf0 = static_cast<int32_t>(g.leaf0);
     a.n_leaves = static_cast<int32_t>(g.n_leaves_local);
+    if (static_cast<int64_t>(a.n_pm) * a.n_leaves > INT32_MAX) return RLK_ERR_UNSUPPORTED;
     a.n_items = a.n_pm * a.n_leaves;
     a.n_kb = static_cast<int32_t>(ceil_div(H, f8 ? BK8 : BK));
     if (f8) {
@@ -645,6 +646,12 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return RLK_ERR_WORKSPACE;
   if (workspace_bytes < rlk_linear_logp_bwd_workspace(T, H, V_local)) return RLK_ERR_WORKSPACE;
   if (Vd > INT32_MAX / 2) return RLK_ERR_UNSUPPORTED;
+  // every launch's work-item count fits int32 (checked before anything is enqueued)
+  {
+    const int64_t pm = ceil_div(T, PAIR_M), nt = ceil_div(H, BN);
+    if ((Vd / BN) * pm > INT32_MAX || pm * nt > INT32_MAX || ceil_div(V_local, PAIR_M) * nt > INT32_MAX)
+      return RLK_ERR_UNSUPPORTED;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint16_t* dz = static_cast<uint16_t*>(workspace);
   const int32_t n_pm = static_cast<int32_t>(ceil_div(T, PAIR_M));
@@ -683,6 +690,7 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
     a.vocab_start = static_cast<int32_t>(vocab_start);
     a.V_true = static_cast<int32_t>(V_true);
     a.n_pm = n_pm;
+    if ((Vd / BN) * static_cast<int64_t>(n_pm) > INT32_MAX) return RLK_ERR_UNSUPPORTED;
     a.n_items = static_cast<int32_t>(Vd / BN) * n_pm;
     a.n_kb = static_cast<int32_t>(ceil_div(H, f8 ? BK8 : BK));
     if (f8) {
@@ -713,6 +721,7 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
       a.H = static_cast<int32_t>(H);
       a.n_mt = n_pm;
       a.n_nt = static_cast<int32_t>(ceil_div(H, BN));
+      if (static_cast<int64_t>(a.n_mt) * a.n_nt > INT32_MAX) return RLK_ERR_UNSUPPORTED;
       a.n_items = a.n_mt * a.n_nt;
       a.n_kb = static_cast<int32_t>(ceil_div(V_valid, BK));
       a.out = dH;
@@ -738,6 +747,7 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
     a.H = static_cast<int32_t>(H);
     a.n_mt = static_cast<int32_t>(ceil_div(V_local, PAIR_M));
     a.n_nt = static_cast<int32_t>(ceil_div(H, BN));
+    if (static_cast<int64_t>(a.n_mt) * a.n_nt > INT32_MAX) return RLK_ERR_UNSUPPORTED;
     a.n_items = a.n_mt * a.n_nt;
     a.n_kb = static_cast<int32_t>(ceil_div(T, BK));
     a.out = dW;
