@@ -410,6 +410,10 @@ size_t fwd_ws_array_bytes(int64_t T, int64_t V_local) {
   return static_cast<size_t>(round_up(ceil_div(V_local, LEAF) * T * 4, 256));
 }
 
+// Work-item counters of the tile kernels (one int32 per launch of a call; each launch
+// zeroes its own before it starts), at the end of either workspace.
+constexpr size_t SCHED_BYTES = 256;
+
 // Backward workspace: the bf16 dz tiles, then (when dH's K = vocab spans several
 // accumulation chunks) an fp32 running sum for a bf16 dH.
 size_t bwd_dz_bytes(int64_t T, int64_t V_local) {
@@ -459,7 +463,7 @@ const char* rlk_status_string(rlk_status s) {
 size_t rlk_linear_logp_fwd_workspace(int64_t T, int64_t H, int64_t V_local) {
   (void)H;
   if (T <= 0 || V_local <= 0) return 0;
-  return 3 * fwd_ws_array_bytes(T, V_local);
+  return 3 * fwd_ws_array_bytes(T, V_local) + SCHED_BYTES;
 }
 
 }  // extern "C"
@@ -492,7 +496,7 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
   const size_t arr = fwd_ws_array_bytes(T, V_local);
   if (g.n_leaves_local > 0) {
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return RLK_ERR_WORKSPACE;
-    if (workspace_bytes < 3 * arr) return RLK_ERR_WORKSPACE;
+    if (workspace_bytes < 3 * arr + SCHED_BYTES) return RLK_ERR_WORKSPACE;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* ws = static_cast<float*>(workspace);  // [T][n_leaves_local][3] (fits in 3 * arr)
@@ -527,6 +531,7 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
       a.pm_out = reinterpret_cast<float*>(static_cast<char*>(p_saved) + saved_probs_offset(T, V_local));
     }
     a.err_flag = err_flag;
+    a.sched = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + 3 * arr);
     a.stall_stage = stall_stage;
     if ((f8 ? launch_gemm_fwd8(maps, a, s) : launch_gemm_fwd(maps, a, s)) != cudaSuccess) return RLK_ERR_CUDA;
   }
@@ -615,7 +620,7 @@ rlk_status rlk_lse_merge(const rlk_lse_partial* partials, int32_t S, int64_t T, 
 
 size_t rlk_linear_logp_bwd_workspace(int64_t T, int64_t H, int64_t V_local) {
   if (T <= 0 || V_local <= 0) return 0;
-  return bwd_dz_bytes(T, V_local) + bwd_run_bytes(T, H, V_local);
+  return bwd_dz_bytes(T, V_local) + bwd_run_bytes(T, H, V_local) + SCHED_BYTES;
 }
 
 }  // extern "C"
@@ -655,6 +660,8 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint16_t* dz = static_cast<uint16_t*>(workspace);
   const int32_t n_pm = static_cast<int32_t>(ceil_div(T, PAIR_M));
+  int32_t* sched = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + bwd_dz_bytes(T, V_local) +
+                                              bwd_run_bytes(T, H, V_local));  // dz, dH, dW
 
   // 1. dz (bf16) workspace: from saved probabilities, saved logits, or recomputed z tiles
   if (p_saved) {
@@ -703,6 +710,7 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
     a.dz = dz;
     a.dz_ld = Vd;
     a.err_flag = err_flag;
+    a.sched = sched;
     if ((f8 ? launch_gemm_dz8(maps, a, s) : launch_gemm_dz(maps, a, s)) != cudaSuccess) return RLK_ERR_CUDA;
   }
 
@@ -732,6 +740,7 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
       if (!dH_fp32_partial && a.n_kb > KC_BLOCKS)
         a.acc_scratch = reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_dz_bytes(T, V_local));
       a.err_flag = err_flag;
+      a.sched = sched + 1;
       if (launch_gemm_dh(maps, a, s) != cudaSuccess) return RLK_ERR_CUDA;
     }
   }
@@ -756,6 +765,7 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
     a.out_cols = static_cast<int32_t>(H);
     a.out_f32 = 1;
     a.err_flag = err_flag;
+    a.sched = sched + 2;
     if (launch_gemm_dw(maps, a, s) != cudaSuccess) return RLK_ERR_CUDA;
   }
   return RLK_OK;

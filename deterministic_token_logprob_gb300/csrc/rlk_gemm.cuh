@@ -31,9 +31,10 @@
 //   warps 2-5  epilogue in each CTA: tcgen05.ld of its own 128 accumulator rows
 //              (thread = row, lane quarter = warp % 4) -> registers -> mode math ->
 //              global memory; releases the accumulator on the even CTA's barrier.
-// Work items are assigned statically (item = cluster + i * clusters), so numerics
-// never depend on the grid: each output element is produced by one fixed
-// instruction sequence regardless of T, batch composition or SM count.
+// Work items are handed out at run time in ascending index order (ItemRing below).
+// Which cluster computes an item, and when, never changes its arithmetic: each output
+// element is produced by one fixed instruction sequence regardless of T, batch
+// composition, SM count or scheduling.
 #pragma once
 
 #include <atomic>
@@ -63,11 +64,18 @@ struct Operands {
 // pairs, vocab unit = leaf (forward) or 256-column tile (dz). Token pair-tiles are taken in
 // groups of TOKEN_GROUP; inside a group the items run vocab-unit-major, so the clusters
 // working at one time touch at most TOKEN_GROUP token tiles of h (32 MiB of bf16 h at
-// H = 4096). Measured on the fwd+bwd step at T = 8192 (power-capped): groups of 16 are ~1.3 %
-// faster than one group of all 32 token tiles; groups of 8 and 4 are 3 % and 4 % slower
-// (each extra group streams W again). The order changes only which cluster computes a tile
-// and when, never a tile's arithmetic.
+// H = 4096), and W is streamed once per group. Measured at T = 8192 (GB300, items handed
+// out in order): groups of 16 read 3.4 GB (forward) and 2.6 GB (dz) from DRAM; one group of
+// all 32 token tiles read 9.4 / 7.7 GB (64 MiB of h does not stay in L2) and made the
+// power-capped fwd+bwd step 3 % slower. The order changes only which cluster computes a
+// tile and when, never a tile's arithmetic.
 constexpr int TOKEN_GROUP = 16;
+// dH / dW work order: items are (row tile, column tile) pairs of the output, column tiles
+// taken in groups of COL_GROUP, row-tile-major inside a group. Measured at T = 8192,
+// H = 4096 (16 column tiles): groups of 8 read 15.3 GB (dH) and 6.3 GB (dW) from DRAM,
+// all 16 in one group 23.3 / 8.8 GB, groups of 4 15.4 / 10.1 GB; groups of 8 made the
+// power-capped fwd+bwd step 1.6 % faster than one group.
+constexpr int COL_GROUP = 8;
 
 __device__ __forceinline__ void item_unit_pm(const GemmArgs& a, int n_units, int item, int& unit, int& pm) {
   const int g0 = (item / (TOKEN_GROUP * n_units)) * TOKEN_GROUP;  // first token tile of the group
@@ -113,17 +121,18 @@ __device__ __forceinline__ void tile_origin(const GemmArgs& a, int item, int j, 
     m0 = pm * PAIR_M;
     n0 = vt * BN;
   } else {
-    const int mt = item / a.n_nt, nt = item % a.n_nt;
-    m0 = mt * PAIR_M;
-    n0 = nt * BN;
+    // dH / dW: output column tiles in groups of COL_GROUP, row-tile-major inside a group
+    const int g0 = (item / (COL_GROUP * a.n_mt)) * COL_GROUP;  // first column tile of the group
+    const int gsize = min(COL_GROUP, a.n_nt - g0);
+    const int r = item - g0 * a.n_mt;
+    m0 = (r / gsize) * PAIR_M;
+    n0 = (g0 + r % gsize) * BN;
   }
 }
 
 // Shared state of one CTA of the pair.
 struct PairCtx {
   uint32_t rank;           // 0 = even CTA (issues the MMAs), 1 = odd CTA
-  uint32_t cluster;        // cluster index
-  uint32_t n_clusters;
   volatile int* abort_flag;
   uint32_t peer_abort;     // shared::cluster address of the peer CTA's abort flag
 };
@@ -152,6 +161,70 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
 }
 
 // ---------------------------------------------------------------------------
+// Work-item hand-out. The even CTA's producer draws the next item index from a
+// counter in global memory (zeroed before the launch) each time it is ready to load
+// another item, so the items in flight across all clusters always form one
+// contiguous window of the work order, and the operand tiles they share are fetched
+// while they are still in L2 however far the clusters drift apart in speed. (With a
+// fixed round-robin assignment, clusters that run slightly faster move ahead into
+// items whose operands no other cluster is reading, and the shared tiles are fetched
+// from DRAM several times.) The index reaches the other roles of both CTAs through a
+// ring of shared-memory slots: `full[s]` (in each CTA, one arrival from the even
+// producer) publishes slot s, `empty[s]` (in the even CTA) collects one release from
+// every reader: the odd producer, the MMA issuer and the eight epilogue warps. An
+// index of -1 ends the work.
+// ---------------------------------------------------------------------------
+constexpr uint32_t ITEM_READERS = 1 + 1 + 4 * PAIR;
+
+struct ItemRing {
+  uint64_t* full;   // [ITEM_RING]
+  uint64_t* empty;  // [ITEM_RING], used in the even CTA only
+  int* slot;        // [ITEM_RING]
+  uint32_t seq = 0;
+};
+
+// Even producer: draw the next item and publish it to both CTAs. False on abort.
+__device__ __forceinline__ bool ring_publish(const GemmArgs& a, ItemRing& q, const PairCtx& c, int& item) {
+  const uint32_t s = q.seq % ITEM_RING, ph = (q.seq / ITEM_RING) & 1u;
+  if (!pair_wait(&q.empty[s], ph ^ 1u, c)) return false;  // every reader took the slot's last index
+  int v = atomicAdd(a.sched, 1);
+  if (v >= a.n_items) v = -1;
+  const uint32_t slot_addr = smem_u32(&q.slot[s]);
+  const uint32_t full_addr = smem_u32(&q.full[s]);
+  st_cluster_u32(map_to_cta(slot_addr, 0u), static_cast<uint32_t>(v));
+  st_cluster_u32(map_to_cta(slot_addr, 1u), static_cast<uint32_t>(v));
+  mbar_arrive_cluster(map_to_cta(full_addr, 0u));  // release: the stores above come first
+  mbar_arrive_cluster(map_to_cta(full_addr, 1u));
+  ++q.seq;
+  item = v;
+  return true;
+}
+
+// Any other reader (one thread): take the next published item and release its slot.
+__device__ __forceinline__ bool ring_take(ItemRing& q, const PairCtx& c, int& item) {
+  const uint32_t s = q.seq % ITEM_RING, ph = (q.seq / ITEM_RING) & 1u;
+  if (!pair_wait(&q.full[s], ph, c)) return false;
+  item = *reinterpret_cast<volatile int*>(&q.slot[s]);
+  mbar_arrive_cluster(map_to_cta(smem_u32(&q.empty[s]), 0u));
+  ++q.seq;
+  return true;
+}
+
+// An epilogue warp: every lane takes the item; lane 0 releases the slot once the whole
+// warp has read it. False (in every lane) on abort.
+__device__ __forceinline__ bool ring_take_warp(ItemRing& q, const PairCtx& c, int& item) {
+  const uint32_t s = q.seq % ITEM_RING, ph = (q.seq / ITEM_RING) & 1u;
+  bool got = pair_wait(&q.full[s], ph, c);
+  got = __all_sync(0xffffffffu, got);
+  if (!got) return false;
+  item = *reinterpret_cast<volatile int*>(&q.slot[s]);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&q.empty[s]), 0u));
+  ++q.seq;
+  return true;
+}
+
+// ---------------------------------------------------------------------------
 // warp 0: TMA producer (one thread per CTA)
 // ---------------------------------------------------------------------------
 constexpr int A_BOX_ROWS = 64;                    // K-major A boxes: 64 rows x 64 K
@@ -176,8 +249,8 @@ __device__ __forceinline__ void load_mn_tile(uint8_t* dst, const CUtensorMap* m,
 }
 
 template <int MODE>
-__device__ void producer_loop(const TileMaps& maps, const GemmArgs& a,
-                              uint8_t* smem, uint64_t* full, uint64_t* empty, const PairCtx& c) {
+__device__ void producer_loop(const TileMaps& maps, const GemmArgs& a, uint8_t* smem, uint64_t* full,
+                              uint64_t* empty, ItemRing ring, const PairCtx& c) {
   // L2 policy per operand: h is re-read by every leaf / vocab tile (fwd, dz) or by
   // every vocab tile of dW, so it is kept; the W tiles of fwd / dz are used by all
   // token tiles within a short window and then never again, so they go first.
@@ -191,7 +264,10 @@ __device__ void producer_loop(const TileMaps& maps, const GemmArgs& a,
   const uint32_t r = c.rank;
   uint32_t issued = 0;
   bool ok = true;
-  for (int item = c.cluster; ok && item < a.n_items; item += c.n_clusters) {
+  while (ok) {
+    int item;
+    ok = (r == 0) ? ring_publish(a, ring, c, item) : ring_take(ring, c, item);
+    if (!ok || item < 0) break;
     const int ntiles = item_tiles<MODE>(a, item);
     for (int j = 0; ok && j < ntiles; ++j) {
       int m0, n0;
@@ -265,12 +341,15 @@ __device__ void producer_loop(const TileMaps& maps, const GemmArgs& a,
 template <int MODE>
 __device__ void mma_loop(const GemmArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
                          uint64_t* acc_full, uint64_t* acc_empty, uint64_t* drain,
-                         uint32_t tmem_base, const PairCtx& c) {
+                         uint32_t tmem_base, ItemRing ring, const PairCtx& c) {
   using Ops = Operands<MODE>;
   uint32_t it = 0, tile = 0;
   bool ok = true;
   const int nchunks = tile_chunks<MODE>(a);
-  for (int item = c.cluster; ok && item < a.n_items; item += c.n_clusters) {
+  while (ok) {
+    int item;
+    ok = ring_take(ring, c, item);
+    if (!ok || item < 0) break;
     const int ntiles = item_tiles<MODE>(a, item) * nchunks;  // accumulator fills of this item
     for (int j = 0; ok && j < ntiles; ++j) {
       const uint32_t buf = tile & 1u, use = tile >> 1;
@@ -440,7 +519,7 @@ __device__ __forceinline__ void apply_row_col_scales(float (&v)[64], float s_row
 
 template <int MODE>
 __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* acc_empty,
-                              uint32_t tmem_base, const PairCtx& c) {
+                              uint32_t tmem_base, ItemRing ring, const PairCtx& c) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;  // TMEM lane quarter this warp may access
   const int row = quarter * 32 + lane;
@@ -450,7 +529,10 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
   bool ok = true;
 
   const int nchunks = tile_chunks<MODE>(a);
-  for (int item = c.cluster; ok && item < a.n_items; item += c.n_clusters) {
+  while (ok) {
+    int item;
+    ok = ring_take_warp(ring, c, item);
+    if (!ok || item < 0) break;
     const int ntiles = item_tiles<MODE>(a, item) * nchunks;  // accumulator fills of this item
     int m0, n0;
     tile_origin<MODE>(a, item, 0, m0, n0);
@@ -646,14 +728,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  ItemRing ring;
+  ring.full = drain + 1;
+  ring.empty = ring.full + ITEM_RING;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ring.empty + ITEM_RING);
   int* abort_word = reinterpret_cast<int*>(tmem_slot + 1);
+  ring.slot = abort_word + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   PairCtx c;
   c.rank = cluster_ctarank();
-  c.cluster = blockIdx.x / PAIR;
-  c.n_clusters = gridDim.x / PAIR;
   c.abort_flag = abort_word;
   c.peer_abort = map_to_cta(smem_u32(abort_word), c.rank ^ 1u);
 
@@ -667,6 +751,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&acc_empty[b], PAIR * 4);  // one arrival per epilogue warp of both CTAs
     }
     mbar_init(drain, 1);
+    for (int i = 0; i < ITEM_RING; ++i) {
+      mbar_init(&ring.full[i], 1);              // the even producer's publication
+      mbar_init(&ring.empty[i], ITEM_READERS);  // even CTA: one release per reader
+    }
     *abort_word = 0;
     fence_mbar_init();
   }
@@ -686,12 +774,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) producer_loop<MODE>(maps, a, smem, full, empty, c);
+    if (lane == 0) producer_loop<MODE>(maps, a, smem, full, empty, ring, c);
   } else if (warp == 1) {
     if (lane == 0 && c.rank == 0)
-      mma_loop<MODE>(a, smem, full, empty, acc_full, acc_empty, drain, tmem_base, c);
+      mma_loop<MODE>(a, smem, full, empty, acc_full, acc_empty, drain, tmem_base, ring, c);
   } else {
-    epilogue_loop<MODE>(a, acc_full, acc_empty, tmem_base, c);
+    epilogue_loop<MODE>(a, acc_full, acc_empty, tmem_base, ring, c);
   }
 
   tc_fence_before();
@@ -739,6 +827,9 @@ cudaError_t launch_gemm(const TileMaps& maps, const GemmArgs& a,
   }
   clusters = min(clusters, a.n_items);
   cfg.gridDim = dim3(PAIR * clusters, 1, 1);
+  if (!a.sched) return cudaErrorInvalidValue;
+  e = cudaMemsetAsync(a.sched, 0, sizeof(int32_t), stream);  // the work-item counter
+  if (e != cudaSuccess) return e;
   e = cudaLaunchKernelEx(&cfg, kernel, maps, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -38,7 +38,10 @@ constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int MN_ATOM_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) TMA box, 8 KiB
 constexpr int NUM_THREADS = 192;            // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int TMEM_COLS = 512;              // two fp32 128x256 accumulators per CTA
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /* alignment slack */ + 256 /* barriers */;
+// Work items reach the roles of a pair through a ring of ITEM_RING shared-memory slots
+// (the even CTA's producer draws them from a counter in global memory).
+constexpr int ITEM_RING = 8;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /* alignment slack */ + 512 /* barriers, slots */;
 
 enum GemmMode : int {
   MODE_FWD = 0,  // z = h W^T per (token tile, leaf): online max / sum-exp / target
@@ -64,7 +67,7 @@ constexpr int BK8 = 128;
 // tile) or, when its row length is a multiple of 64 elements, a 3-D view
 // {64 elements, K rows, row / 64 atoms} that fetches both 64-wide swizzle atoms of the
 // tile in one copy; the shared-memory image is the same.
-struct alignas(64) TileMaps {
+struct TileMaps {  // CUtensorMap is 128-byte aligned, as TMA descriptors must be (64 B at least)
   CUtensorMap a, a_full, b;
 };
 
@@ -72,6 +75,7 @@ struct GemmArgs {
   int32_t T = 0, H = 0;
   int32_t n_items = 0;
   int32_t n_kb = 0;  // k-blocks of BK per tile
+  int32_t* sched = nullptr;  // work-item counter in global memory; the launcher zeroes it
   int32_t* err_flag = nullptr;
   // forward / dz
   int32_t V_local = 0, vocab_start = 0, V_true = 0;

@@ -9,8 +9,10 @@
 // with cudaGetSymbolAddress and cached.
 //
 // All calls on a device share this one array and it keeps the previous call's
-// contents. Nothing in it needs to start at zero: the forward's tile kernel writes
-// every (leaf, token) entry that the merge kernel then reads. Two calls whose work
+// contents. The one part that must start at zero, the tile kernel's work-item
+// counter at the end of the workspace, is zeroed on the stream by every call before
+// its kernel runs; the tile kernel writes every (leaf, token) entry that the merge
+// kernel then reads. Two calls whose work
 // overlaps on the GPU (e.g. on different streams without ordering between them)
 // race on the array and produce wrong results; order them.
 #include <cuda_runtime.h>

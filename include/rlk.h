@@ -27,7 +27,9 @@
  *  2. Partitioning: the hidden dimension is reduced in steps of 64 (one K=16
  *     tensor-core instruction at a time, ascending). The vocabulary is cut into
  *     leaves of RLK_LEAF_WIDTH = 1024 global columns, each walked in 256-column
- *     tiles in ascending order. No split-K, no atomics.
+ *     tiles in ascending order. No split-K, no atomics on data (one atomic
+ *     counter per launch only hands out work items; which CTA pair computes an
+ *     output tile never changes how it is computed).
  *  3. Merge order: leaves are merged by a balanced pairwise tree defined on
  *     global leaf indices: nLeaves = ceil(V_true / 1024) leaves are grouped into
  *     RLK_MAX_SHARDS = 8 super-shards of L = ceil(nLeaves / 8) leaves; inside a
@@ -113,7 +115,9 @@ typedef struct {
   float zt;
 } rlk_lse_partial;
 
-/* Bytes of device workspace rlk_linear_logp_fwd needs (256-byte aligned base). */
+/* Bytes of device workspace rlk_linear_logp_fwd needs (256-byte aligned base): the
+ * per-(token, leaf) statistics, then 256 bytes of work-item counters that the call
+ * zeroes on its stream before its kernels use them. */
 RLK_API size_t rlk_linear_logp_fwd_workspace(int64_t T, int64_t H, int64_t V_local);
 
 /*
@@ -160,7 +164,8 @@ RLK_API rlk_status rlk_lse_merge(const rlk_lse_partial* partials, int32_t S, int
 /* Bytes of device workspace rlk_linear_logp_bwd needs: the bf16 dz tile store
  * [T][round_up(V_local, 256)] (the "controlled workspace" of the fourth reason
  * in "Why the Fused Path Wins"), plus, when V_local > 65536, an fp32 [T][H]
- * running sum for dH's chunked accumulation. */
+ * running sum for dH's chunked accumulation, plus 256 bytes of work-item counters
+ * (zeroed by the call on its stream). */
 RLK_API size_t rlk_linear_logp_bwd_workspace(int64_t T, int64_t H, int64_t V_local);
 
 /*

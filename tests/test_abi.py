@@ -56,13 +56,15 @@ def test_version_and_status_strings(lib):
 
 
 def test_workspace_queries(lib):
-    # forward: three fp32 arrays of ceil(V_local/1024) x T, each rounded up to 256 bytes
+    # forward: three fp32 arrays of ceil(V_local/1024) x T, each rounded up to 256 bytes,
+    # then 256 bytes of work-item counters
     T, V = 4096, 151936
     per = -(-(V // 1024 + (V % 1024 > 0)) * T * 4 // 256) * 256
-    assert lib.rlk_linear_logp_fwd_workspace(T, 4096, V) == 3 * per
+    assert lib.rlk_linear_logp_fwd_workspace(T, 4096, V) == 3 * per + 256
     # backward: bf16 dz tiles [T][round_up(V_local, 256)] + fp32 [T][H] running sum of dH
-    assert lib.rlk_linear_logp_bwd_workspace(T, 4096, V) == T * 152064 * 2 + T * 4096 * 4
-    assert lib.rlk_linear_logp_bwd_workspace(T, 4096, 16384) == T * 16384 * 2  # one chunk
+    # + the counters
+    assert lib.rlk_linear_logp_bwd_workspace(T, 4096, V) == T * 152064 * 2 + T * 4096 * 4 + 256
+    assert lib.rlk_linear_logp_bwd_workspace(T, 4096, 16384) == T * 16384 * 2 + 256  # one chunk
     assert lib.rlk_linear_logp_fwd_workspace(0, 4096, V) == 0
     assert lib.rlk_linear_logp_bwd_workspace(0, 4096, V) == 0
 
