@@ -174,7 +174,9 @@ def run_reference(args, w: workloads.Workload, rank: int, world: int):
     d = workloads.make_inputs(w)
     import oracle
     oracle.build()
-    n_tok = min(w.T, 2 * oracle.default_threads())   # a bounded sample per step (a few seconds)
+    # a bounded sample per step (about 10 s): 8 tokens per host thread, the block of tokens
+    # the oracle's forward and dH widen each W row for, as in the GPU arm's cpu_baseline
+    n_tok = min(w.T, 8 * oracle.default_threads())
     for i in range(args.warmup):
         oracle_sample_rate(w, d, n_tok=min(n_tok, 4), n_vrows=64, seed=100 + i)
     rates = []
