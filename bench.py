@@ -17,6 +17,7 @@ step a bounded sample of the same workload, extrapolated per token).
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -75,53 +76,71 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling (every 200 ms) of SM clock and throttle reasons while running."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples (every 50 ms) of SM clock, power and throttle reasons. Only samples
+    whose timestamps fall between mark_start() and mark_end() (the timed region) are kept."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, gpu_id: str):
+    def __init__(self, gpu_id: str, interval_ms: int = 50):
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
         try:
             fd, self.path = tempfile.mkstemp(prefix="rlk_clocks_", suffix=".csv")
             self.out = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", gpu_id], stdout=self.out, stderr=subprocess.DEVNULL)
+                 "-lms", str(interval_ms), "-i", gpu_id], stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def wait_running(self, timeout_s: float = 5.0):
+        """Return once the first sample has been written (or after timeout_s)."""
+        t_end = time.time() + timeout_s
+        while self.proc is not None and time.time() < t_end:
+            if os.path.getsize(self.path) > 0:
+                return
+            time.sleep(0.02)
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def stop(self):
         if self.proc is None:
             return None
-        time.sleep(0.25)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.out.close()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        samples = []
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    samples.append((ts, float(parts[2]), float(parts[3]),
+                                    [n for n, v in zip(self.REASONS, parts[6:10])
+                                     if v.lower().startswith("active")]))
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
         os.unlink(self.path)
-        if not sm:
+        inside = [x for x in samples if self.t0 is not None and self.t1 is not None
+                  and self.t0 <= x[0] <= self.t1]
+        use = inside or samples
+        if not use:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        return {"sm_mhz": statistics.median(x[1] for x in use), "sm_max_mhz": max(x[2] for x in use),
+                "samples": len(use), "samples_in_timed_region": bool(inside),
+                "reasons": sorted({r for x in use for r in x[3]})}
 
 
 # ----------------------------------------------------------------------------- oracle timing
@@ -330,10 +349,14 @@ def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     sampler = ClockSampler(gpu_uuid(torch, device)) if rank == 0 else None
+    if sampler:
+        sampler.wait_running()
     barrier()
     torch.cuda.synchronize(device)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.mark_start()
     t_start.record(stream)
     for i in range(K):
         ev[i][0].record(stream)
@@ -343,6 +366,8 @@ def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int)
         ev[i][2].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(device)
+    if sampler:
+        sampler.mark_end()
     barrier()
     clocks = sampler.stop() if sampler else None
     total_ms = t_start.elapsed_time(t_end)

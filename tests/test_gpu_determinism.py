@@ -65,6 +65,25 @@ def test_stream_and_concurrent_work_do_not_change_bits(rlk):
         assert torch.equal(a, b)
 
 
+def test_two_calls_running_at_once_on_two_streams(rlk):
+    # Each call hands out its work items from a counter in its own workspace; two calls whose
+    # kernels overlap on the GPU (so neither has all SMs) must not disturb each other.
+    w, d, h, W, y, g = _mid()
+    ref = _all_outputs(rlk, w, h, W, y, g)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [[], []]
+    for rep in range(3):
+        for i, st in enumerate(streams):
+            with torch.cuda.stream(st):
+                outs[i].append(_all_outputs(rlk, w, h, W, y, g, stream=st))
+    torch.cuda.synchronize()
+    for per_stream in outs:
+        for got in per_stream:
+            for a, b in zip(ref, got):
+                assert torch.equal(a, b)
+
+
 def _invariance(rlk, H, V, Vt, W_bits, W_dev, Ts, oracle_mod=None, check_dH=True):
     th, ty = workloads.invariance_targets(0, H=H, V_true=Vt)
     n = th.shape[0]
