@@ -396,6 +396,7 @@ def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int)
                      "frac": achieved / peak,
                      "traffic": fwd_traffic_per_launch() if w.name == "qwen3_8b" else None,
                      "peak_source": f"{peaks_src} bf16 burst",
+                     "frac_of_sustained": achieved / peak_sus,
                      "algorithmic_flops_per_launch": flops_fwd, "avg_launch_ms": fwd_avg},
         "step_roofline": {"flops_counted": step_flops, "roofline_ms": roofline_ms,
                           "frac_of_burst": roofline_ms / ms_per_step,

@@ -306,7 +306,9 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
   cuuint64_t strides[1] = {row_elems * static_cast<uint64_t>(elem_bytes)};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType dt = elem_bytes == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box,
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -343,6 +345,12 @@ bool encode_rows(TileMaps* m, const void* base, uint64_t row_elems, uint64_t T, 
   const uint32_t k_box = 128u / static_cast<uint32_t>(elem_bytes);
   return encode_2d(&m->a, base, row_elems, T, row_elems, k_box, 64, elem_bytes) &&
          encode_2d(&m->a_full, base, row_elems, T, row_elems, k_box, BM, elem_bytes);
+}
+
+// Output [rows][cols] (row length cols, contiguous) as TileMaps::out: boxes of 128 bytes
+// (64 bf16 or 32 fp32 columns) x 32 rows, 128-byte swizzle, for the epilogue's TMA stores.
+bool encode_out(TileMaps* m, const void* base, uint64_t cols, uint64_t rows, int elem_bytes) {
+  return encode_2d(&m->out, base, cols, rows, cols, 128u / static_cast<uint32_t>(elem_bytes), 32, elem_bytes);
 }
 
 // E4M3 operands of the FP8 entry points: codes in place of h / W plus their scales.
@@ -503,7 +511,7 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
 
   if (g.n_leaves_local > 0) {
     const int eb = f8 ? 1 : 2;  // element bytes of h / W
-    TileMaps maps;
+    TileMaps maps{};
     if (!encode_rows(&maps, h, H, T, eb)) return RLK_ERR_CUDA;
     if (!encode_2d(&maps.b, W, H, V_local, H, 128 / eb, B_HALF, eb)) return RLK_ERR_CUDA;
     GemmArgs a;
@@ -687,7 +695,7 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
     if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
   } else {
     const int eb = f8 ? 1 : 2;  // element bytes of the logit operands
-    TileMaps maps;
+    TileMaps maps{};
     if (!encode_rows(&maps, f8 ? hq : h, H, T, eb)) return RLK_ERR_CUDA;
     if (!encode_2d(&maps.b, f8 ? Wq : W, H, V_local, H, 128 / eb, B_HALF, eb)) return RLK_ERR_CUDA;
     GemmArgs a;
@@ -709,6 +717,8 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
     a.g = g;
     a.dz = dz;
     a.dz_ld = Vd;
+    if (!encode_out(&maps, dz, Vd, T, 2)) return RLK_ERR_CUDA;
+    a.out_tma = 1;
     a.err_flag = err_flag;
     a.sched = sched;
     if ((f8 ? launch_gemm_dz8(maps, a, s) : launch_gemm_dz(maps, a, s)) != cudaSuccess) return RLK_ERR_CUDA;
@@ -721,7 +731,7 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
     if (V_valid == 0) {
       if (cudaMemsetAsync(dH, 0, static_cast<size_t>(T) * H * elem, s) != cudaSuccess) return RLK_ERR_CUDA;
     } else {
-      TileMaps maps;
+      TileMaps maps{};
       GemmArgs a;
       if (!encode_rows(&maps, dz, Vd, T)) return RLK_ERR_CUDA;
       if (!encode_mn(&maps.b, W, H, V_local, &a.b_mn_wide)) return RLK_ERR_CUDA;
@@ -739,6 +749,12 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
       a.out_f32 = dH_fp32_partial ? 1 : 0;
       if (!dH_fp32_partial && a.n_kb > KC_BLOCKS)
         a.acc_scratch = reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_dz_bytes(T, V_local));
+      // TMA stores of the final values, unless the fp32 output is itself the running sum
+      // of several K chunks (then every chunk updates it with plain loads and stores)
+      if (!dH_fp32_partial || a.n_kb <= KC_BLOCKS) {
+        if (!encode_out(&maps, dH, H, T, dH_fp32_partial ? 4 : 2)) return RLK_ERR_CUDA;
+        a.out_tma = 1;
+      }
       a.err_flag = err_flag;
       a.sched = sched + 1;
       if (launch_gemm_dh(maps, a, s) != cudaSuccess) return RLK_ERR_CUDA;
@@ -747,7 +763,7 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
 
   // 3. dW = dz^T h (rows at or above V_true come out exactly zero: their dz is zero)
   if (dW) {
-    TileMaps maps;
+    TileMaps maps{};
     GemmArgs a;
     if (!encode_mn(&maps.a, dz, Vd, T, &a.a_mn_wide)) return RLK_ERR_CUDA;
     maps.a_full = maps.a;  // unused: dW's A is MN-major
@@ -764,6 +780,10 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
     a.out_rows = static_cast<int32_t>(V_local);
     a.out_cols = static_cast<int32_t>(H);
     a.out_f32 = 1;
+    if (a.n_kb <= KC_BLOCKS) {  // one K chunk: TMA stores (several: dW is the running sum)
+      if (!encode_out(&maps, dW, H, V_local, 4)) return RLK_ERR_CUDA;
+      a.out_tma = 1;
+    }
     a.err_flag = err_flag;
     a.sched = sched + 2;
     if (launch_gemm_dw(maps, a, s) != cudaSuccess) return RLK_ERR_CUDA;

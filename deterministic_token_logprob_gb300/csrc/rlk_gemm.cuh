@@ -30,7 +30,9 @@
 //              multicast tcgen05.commit.
 //   warps 2-5  epilogue in each CTA: tcgen05.ld of its own 128 accumulator rows
 //              (thread = row, lane quarter = warp % 4) -> registers -> mode math ->
-//              global memory; releases the accumulator on the even CTA's barrier.
+//              global memory (dz, dH, dW: staged per warp in shared memory and written
+//              by TMA stores, BoxStager); releases the accumulator on the even CTA's
+//              barrier.
 // Work items are handed out at run time in ascending index order (ItemRing below).
 // Which cluster computes an item, and when, never changes its arithmetic: each output
 // element is produced by one fixed instruction sequence regardless of T, batch
@@ -517,9 +519,51 @@ __device__ __forceinline__ void apply_row_col_scales(float (&v)[64], float s_row
   }
 }
 
+// Epilogue stores through shared memory and TMA (dz, and the final values of dH / dW):
+// each epilogue warp writes a box of its 32 rows x 128 bytes into one of its two staging
+// buffers (128-byte swizzle: 16-byte chunk j of row r goes to chunk position j ^ (r & 7),
+// the layout the output tensor map expects), and lane 0 stores the box with one TMA copy,
+// which writes whole 128-byte row segments instead of each thread's scattered 16-byte
+// pieces. A buffer is refilled only after the copy that read it two boxes earlier has
+// finished reading it.
+struct BoxStager {
+  uint32_t base;  // shared address of this warp's two buffers
+  uint32_t seq;   // boxes staged so far
+};
+
+__device__ __forceinline__ uint32_t stage_begin(BoxStager& S, int lane) {
+  if (S.seq >= 2) {
+    if (lane == 0) bulk_wait_group_read<1>();
+    __syncwarp();
+  }
+  return S.base + (S.seq & 1u) * STORE_BOX_BYTES;
+}
+
+__device__ __forceinline__ void stage_chunk(uint32_t buf, int lane, int j, uint4 v) {
+  st_shared_v4(buf + static_cast<uint32_t>(lane * 128 + ((j ^ (lane & 7)) << 4)), v);
+}
+
+// Every lane of the warp calls it after staging its row; (x, y) = the box's first column
+// and row in the output.
+__device__ __forceinline__ void stage_store(BoxStager& S, uint32_t buf, int lane, const CUtensorMap* m,
+                                            int x, int y, uint64_t pol) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(m, buf, x, y, pol);
+    bulk_commit_group();
+  }
+  ++S.seq;
+}
+
+__device__ __forceinline__ uint4 f32x4_bits(const float* v) {
+  return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+}
+
 template <int MODE>
 __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* acc_empty,
-                              uint32_t tmem_base, ItemRing ring, const PairCtx& c) {
+                              uint32_t tmem_base, ItemRing ring, const PairCtx& c,
+                              const CUtensorMap* out_map, uint8_t* stage_smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;  // TMEM lane quarter this warp may access
   const int row = quarter * 32 + lane;
@@ -527,6 +571,8 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
   const uint64_t pol_out = policy_evict_first();  // outputs are streamed, never re-read here
   uint32_t tile = 0;
   bool ok = true;
+  BoxStager stg{smem_u32(stage_smem + (warp - 2) * 2 * STORE_BOX_BYTES), 0u};
+  const int row0_off = static_cast<int>(c.rank) * BM + quarter * 32;  // warp's first row in a tile
 
   const int nchunks = tile_chunks<MODE>(a);
   while (ok) {
@@ -607,7 +653,6 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
         const int vcols = max(0, min(min(BN, a.V_true - gc0), a.V_local - n0));
         const int tl = (yvalid && yt >= gc0 && yt < static_cast<int64_t>(gc0) + vcols)
                            ? static_cast<int>(yt - gc0) : -1;
-        uint16_t* dst = a.dz + static_cast<size_t>(t) * a.dz_ld + n0;
         const float ng = -g_t;
 #pragma unroll 1
         for (int ch = 0; ch < BN; ch += 64) {
@@ -635,9 +680,11 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
             for (int i = 0; i < 64; ++i)
               if (i >= valid) v[i] = 0.f;
           }
-          if (t < a.T) {
+          {  // one box: this warp's 32 rows x 64 bf16 columns (rows at or past T are clipped)
+            const uint32_t buf = stage_begin(stg, lane);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) st_global_v4_hint(dst + ch + 8 * q, pack8_bf16(v + 8 * q), pol_out);
+            for (int q = 0; q < 8; ++q) stage_chunk(buf, lane, q, pack8_bf16(v + 8 * q));
+            stage_store(stg, buf, lane, out_map, n0 + ch, m0 + row0_off, pol_out);
           }
         }
       } else {
@@ -675,7 +722,28 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
               continue;
             }
           }
-          if (row_ok && col < a.out_cols) {
+          if (a.out_tma && last) {
+            // the final values (one chunk, or the last chunk folded into the running sum;
+            // `last` is the same for every lane, so the whole warp takes this branch): all
+            // lanes stage their rows, and the copy clips rows and columns past the output
+            if (col < a.out_cols) {
+              if (a.out_f32) {
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                  if (col + 32 * b >= a.out_cols) break;
+                  const uint32_t buf = stage_begin(stg, lane);
+#pragma unroll
+                  for (int q = 0; q < 8; ++q) stage_chunk(buf, lane, q, f32x4_bits(v + 32 * b + 4 * q));
+                  stage_store(stg, buf, lane, out_map, col + 32 * b, m0 + row0_off, pol_out);
+                }
+              } else {
+                const uint32_t buf = stage_begin(stg, lane);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) stage_chunk(buf, lane, q, pack8_bf16(v + 8 * q));
+                stage_store(stg, buf, lane, out_map, col, m0 + row0_off, pol_out);
+              }
+            }
+          } else if (!a.out_tma && row_ok && col < a.out_cols) {
             if (a.out_f32) {
               float* p = static_cast<float*>(a.out) + static_cast<size_t>(t) * a.out_ld + col;
 #pragma unroll
@@ -712,6 +780,10 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
       }
     }
   }
+  // Every TMA store of this warp completes before the CTA may exit: its staging buffers
+  // stay valid while they are read, and its writes are performed.
+  if (lane == 0) bulk_wait_group_all();
+  __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
@@ -723,7 +795,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* stage_smem = smem + STAGES * STAGE_BYTES;  // epilogue store staging (BoxStager)
+  uint64_t* full = reinterpret_cast<uint64_t*>(stage_smem + STORE_STAGE_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* acc_full = empty + STAGES;
   uint64_t* acc_empty = acc_full + 2;
@@ -779,7 +852,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0 && c.rank == 0)
       mma_loop<MODE>(a, smem, full, empty, acc_full, acc_empty, drain, tmem_base, ring, c);
   } else {
-    epilogue_loop<MODE>(a, acc_full, acc_empty, tmem_base, ring, c);
+    epilogue_loop<MODE>(a, acc_full, acc_empty, tmem_base, ring, c, &maps.out, stage_smem);
   }
 
   tc_fence_before();

@@ -41,7 +41,12 @@ constexpr int TMEM_COLS = 512;              // two fp32 128x256 accumulators per
 // Work items reach the roles of a pair through a ring of ITEM_RING shared-memory slots
 // (the even CTA's producer draws them from a counter in global memory).
 constexpr int ITEM_RING = 8;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /* alignment slack */ + 512 /* barriers, slots */;
+// Epilogue store staging: each of the four epilogue warps owns two 4 KiB buffers, each one
+// TMA store box of 32 rows x 128 bytes (128-byte swizzle).
+constexpr int STORE_BOX_BYTES = 32 * 128;
+constexpr int STORE_STAGE_BYTES = 4 * 2 * STORE_BOX_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STORE_STAGE_BYTES + 1024 /* alignment slack */ +
+                           512 /* barriers, slots */;
 
 enum GemmMode : int {
   MODE_FWD = 0,  // z = h W^T per (token tile, leaf): online max / sum-exp / target
@@ -63,12 +68,14 @@ constexpr int BK8 = 128;
 //          (dz of dW): see a_mn_wide
 //  a_full  K-major A: the same tensor in 128-row boxes, for tiles with all rows below T
 //  b       W or h: K-major 64 x 128 boxes (fwd, dz), or MN-major (dH, dW): see b_mn_wide
+//  out     the output of dz / dH / dW for TMA stores: boxes of 128 bytes x 32 rows (64 bf16
+//          or 32 fp32 columns), 128-byte swizzle; used when GemmArgs::out_tma is set
 // An MN-major operand is either a 2-D map with 64 x 64 boxes (two copies per 128-wide
 // tile) or, when its row length is a multiple of 64 elements, a 3-D view
 // {64 elements, K rows, row / 64 atoms} that fetches both 64-wide swizzle atoms of the
 // tile in one copy; the shared-memory image is the same.
 struct TileMaps {  // CUtensorMap is 128-byte aligned, as TMA descriptors must be (64 B at least)
-  CUtensorMap a, a_full, b;
+  CUtensorMap a, a_full, b, out;
 };
 
 struct GemmArgs {
@@ -96,6 +103,7 @@ struct GemmArgs {
   int64_t out_ld = 0;
   int32_t out_rows = 0, out_cols = 0;
   int32_t out_f32 = 0;
+  int32_t out_tma = 0;             // dz / dH / dW: the final values go out by TMA stores (TileMaps::out)
   float* acc_scratch = nullptr;    // dH with bf16 output and several K chunks: fp32 running sum, ld = out_ld
   int32_t a_mn_wide = 0, b_mn_wide = 0;  // MN-major maps are 3-D 128-wide views (TileMaps)
   // E4M3 modes: per-token scale of hq [T] and per-local-row scale of Wq [V_local]
