@@ -443,13 +443,31 @@ def saved_logits_leg(rlk, torch, path, w, device, args, peak, peak_sus):
     b.record()
     torch.cuda.synchronize(device)
     ms = a.elapsed_time(b) / K
+    # the parts: the forward that also stores z, and dz formed from z alone (an HBM-bound
+    # pass: fp32 z of the columns below V_true read, bf16 dz of all padded columns written)
+    fwd_ms = _time_calls(torch, device, lambda: rlk.linear_logp_fwd_save(
+        path.h, path.W, path.y, w.V_true, z_saved=z, out=(path.logp, path.lse), workspace=path.fws), K)
+    dz_ms = _time_calls(torch, device, lambda: rlk.linear_logp_bwd_saved(
+        path.h, path.W, path.y, path.lse, path.g, z, w.V_true, want_dH=False, want_dW=False,
+        out=(None, None), workspace=path.bws), K)
+    dz_bytes = w.T * w.V_true * 4 + w.T * (-(-w.V // 256) * 256) * 2
+    hbm = _peaks_hbm()
     del z
     step_flops = 3.0 * 2.0 * w.T * w.H * w.V_true
     return {"tokens_per_s": w.T / (ms / 1e3), "ms_per_step": ms,
             "frac_of_burst": step_flops / (peak * 1e12) / (ms / 1e3),
             "frac_of_sustained": step_flops / (peak_sus * 1e12) / (ms / 1e3),
             "saved_logits_bytes": rlk.saved_logits_bytes(w.T, w.V), "steps": K,
-            "gpu_launches_per_step": 5}
+            "gpu_launches_per_step": 5,
+            "forward_with_save_ms": fwd_ms,
+            "dz_from_logits": {"ms": dz_ms, "algorithmic_bytes": dz_bytes,
+                               "GBps": dz_bytes / (dz_ms / 1e3) / 1e9,
+                               "frac_of_hbm": dz_bytes / (dz_ms / 1e3) / 1e9 / hbm}}
+
+
+def _peaks_hbm():
+    peaks, _ = load_peaks()
+    return float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
 
 
 def small_t_leg(rlk, torch, path, device, peaks):
@@ -506,11 +524,27 @@ def saved_probs_leg(rlk, torch, path, w, device, args, peak):
     b.record()
     torch.cuda.synchronize(device)
     ms = a.elapsed_time(b) / K
+    # the parts: the forward that also stores the probabilities, and dz formed from them
+    # alone (HBM-bound: bf16 e(z - m) of the columns below V_true and the fp32 chunk maxima
+    # read, bf16 dz of all padded columns written)
+    fwd_ms = _time_calls(torch, device, lambda: rlk.linear_logp_fwd_save_probs(
+        path.h, path.W, path.y, w.V_true, p_saved=pbuf, out=(path.logp, path.lse),
+        workspace=path.fws), K)
+    dz_ms = _time_calls(torch, device, lambda: rlk.linear_logp_bwd_saved_probs(
+        path.h, path.W, path.y, path.lse, path.g, pbuf, w.V_true, want_dH=False, want_dW=False,
+        out=(None, None), workspace=path.bws), K)
+    Vd = -(-w.V // 256) * 256
+    dz_bytes = w.T * w.V_true * 2 + w.T * (Vd // 64) * 4 + w.T * Vd * 2
+    hbm = _peaks_hbm()
     del pbuf
     step_flops = 3.0 * 2.0 * w.T * w.H * w.V_true
     return {"tokens_per_s": w.T / (ms / 1e3), "ms_per_step": ms,
             "frac_of_burst": step_flops / (peak * 1e12) / (ms / 1e3),
-            "saved_probs_bytes": rlk.saved_probs_bytes(w.T, w.V), "steps": K}
+            "saved_probs_bytes": rlk.saved_probs_bytes(w.T, w.V), "steps": K,
+            "forward_with_save_ms": fwd_ms,
+            "dz_from_probs": {"ms": dz_ms, "algorithmic_bytes": dz_bytes,
+                              "GBps": dz_bytes / (dz_ms / 1e3) / 1e9,
+                              "frac_of_hbm": dz_bytes / (dz_ms / 1e3) / 1e9 / hbm}}
 
 
 def _time_calls(torch, device, fn, K, warmup=3):

@@ -497,6 +497,7 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
   if (!partial && (vocab_start != 0 || !g.reaches_end)) return RLK_ERR_INVALID_ARG;
   if (z_saved && (!aligned16(z_saved) || z_saved_bytes < saved_logits_bytes(T, V_local)))
     return RLK_ERR_INVALID_ARG;
+  if (z_saved && p_saved) return RLK_ERR_INVALID_ARG;  // the forward saves one of the two
   if (p_saved && ((reinterpret_cast<uintptr_t>(p_saved) & 255u) != 0 ||
                   p_saved_bytes < saved_probs_bytes(T, V_local)))
     return RLK_ERR_INVALID_ARG;
@@ -534,9 +535,11 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
     a.ws = ws;
     a.z_out = z_saved;
     a.z_ld = round_up(V_local, BN);
+    if (z_saved && !encode_out(&maps, z_saved, a.z_ld, T, 4)) return RLK_ERR_CUDA;
     if (p_saved) {
       a.p_out = static_cast<uint16_t*>(p_saved);
       a.pm_out = reinterpret_cast<float*>(static_cast<char*>(p_saved) + saved_probs_offset(T, V_local));
+      if (!encode_out(&maps, p_saved, a.z_ld, T, 2)) return RLK_ERR_CUDA;
     }
     a.err_flag = err_flag;
     a.sched = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + 3 * arr);

@@ -620,30 +620,29 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
         const int c0 = n0 + a.vocab_start + j * BN;  // global column of the tile's first column
         const int vcols = min(BN, a.V_true - c0);
         const int tl = (yt >= c0 && yt < static_cast<int64_t>(c0) + vcols) ? static_cast<int>(yt - c0) : -1;
-        const size_t lc = static_cast<size_t>(n0 + j * BN);  // local column of the tile
-        float* zrow = (a.z_out && t < a.T) ? a.z_out + static_cast<size_t>(t) * a.z_ld + lc : nullptr;
+        const int lc = n0 + j * BN;  // local column of the tile
         constexpr bool keep_p = (MODE == MODE_FWDP);
 #pragma unroll 1
         for (int ch = 0; ch < BN; ch += 64) {
           float v[64];
           tmem_ld64(taddr + ch, v);
-          if constexpr (is_e4m3<MODE>) apply_row_col_scales(v, s_row, a.b_scale, static_cast<int>(lc) + ch, a.V_local);
-          if (zrow) {  // saved logits: the accumulator exactly as computed
+          if constexpr (is_e4m3<MODE>) apply_row_col_scales(v, s_row, a.b_scale, lc + ch, a.V_local);
+          if (a.z_out) {  // saved logits: the accumulator exactly as computed, two fp32 boxes
 #pragma unroll
-            for (int q = 0; q < 16; ++q)
-              st_global_v4_hint(zrow + ch + 4 * q,
-                                make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
-                                           __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3])),
-                                pol_out);
+            for (int b = 0; b < 2; ++b) {
+              const uint32_t buf = stage_begin(stg, lane);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) stage_chunk(buf, lane, q, f32x4_bits(v + 32 * b + 4 * q));
+              stage_store(stg, buf, lane, out_map, lc + ch + 32 * b, m0 + row0_off, pol_out);
+            }
           }
           if constexpr (keep_p) {  // saved probabilities: bf16 e(z - m) and the fp32 running max m
             fwd_chunk_keep_exps(v, vcols - ch, tl - ch, st);
-            if (t < a.T) {
-              uint16_t* prow = a.p_out + static_cast<size_t>(t) * a.z_ld + lc + ch;
+            const uint32_t buf = stage_begin(stg, lane);
 #pragma unroll
-              for (int q = 0; q < 8; ++q) st_global_v4_hint(prow + 8 * q, pack8_bf16(v + 8 * q), pol_out);
-              a.pm_out[static_cast<size_t>(t) * (a.z_ld / 64) + (lc + ch) / 64] = st.m;
-            }
+            for (int q = 0; q < 8; ++q) stage_chunk(buf, lane, q, pack8_bf16(v + 8 * q));
+            stage_store(stg, buf, lane, out_map, lc + ch, m0 + row0_off, pol_out);
+            if (t < a.T) a.pm_out[static_cast<size_t>(t) * (a.z_ld / 64) + (lc + ch) / 64] = st.m;
           } else {
             fwd_chunk(v, vcols - ch, tl - ch, st);
           }
