@@ -197,83 +197,120 @@ __global__ void shard_sum_kernel(const float* p, int S, int64_t n, uint16_t* out
   }
 }
 
-// dz from saved fp32 logits: eight consecutive columns of one row per thread.
-// Same arithmetic as the recompute epilogue (dz_target / dz_other), so the two
+// dz from saved fp32 logits. One block per token row: the row's target, gradient and lse
+// are read once, and each thread takes eight consecutive columns per step, UNROLL steps
+// at a time with all of their loads issued first (a streaming pass: fp32 z read, bf16 dz
+// written). Same arithmetic as the recompute epilogue (dz_target / dz_other), so the two
 // backward paths produce identical bits.
-__global__ void dz_from_logits_kernel(const float* z, int64_t z_ld, const int64_t* y,
-                                      const float* lse, const float* g, int T, int Vd,
-                                      int V_valid, int vocab_start, int V_true, uint16_t* dz,
-                                      int64_t dz_ld, int32_t* err_flag) {
-  const int64_t groups = static_cast<int64_t>(Vd / 8);
-  const int64_t total = static_cast<int64_t>(T) * groups;
-  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int t = static_cast<int>(idx / groups);
-    const int c0 = static_cast<int>(idx - static_cast<int64_t>(t) * groups) * 8;
-    const int64_t yt = y[t];
-    const bool yvalid = yt >= 0 && yt < V_true;
-    if (!yvalid && c0 == 0 && err_flag) atomicOr(err_flag, RLK_FLAG_BAD_TARGET);
-    float d[8];
+constexpr int DZS_THREADS = 256;
+constexpr int DZS_UNROLL = 4;
+
+__global__ void __launch_bounds__(DZS_THREADS)
+    dz_from_logits_kernel(const float* __restrict__ z, int64_t z_ld, const int64_t* __restrict__ y,
+                          const float* __restrict__ lse, const float* __restrict__ g, int Vd,
+                          int V_valid, int vocab_start, int V_true, uint16_t* __restrict__ dz,
+                          int64_t dz_ld, int32_t* err_flag) {
+  const int t = blockIdx.x;
+  const int64_t yt = y[t];
+  const bool yvalid = yt >= 0 && yt < V_true;
+  if (!yvalid && threadIdx.x == 0 && err_flag) atomicOr(err_flag, RLK_FLAG_BAD_TARGET);
+  const float gt = g[t];
+  const float nl = neg_scaled(lse[t]);
+  const float ng = -gt;
+  const int64_t tcol = yt - vocab_start;  // the target's local column
+  const float* zr = z + static_cast<size_t>(t) * z_ld;
+  uint16_t* dr = dz + static_cast<size_t>(t) * dz_ld;
+  const int n_valid = yvalid ? V_valid : 0;  // columns with a nonzero gradient
+  for (int base = threadIdx.x * 8; base < Vd; base += DZS_THREADS * 8 * DZS_UNROLL) {
+    float4 zv[DZS_UNROLL][2];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) d[i] = 0.f;
-    if (yvalid && c0 < V_valid) {
-      const float4* zp = reinterpret_cast<const float4*>(z + static_cast<size_t>(t) * z_ld + c0);
-      const float4 z0 = zp[0], z1 = zp[1];
-      const float zv[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
-      const float gt = g[t];
-      const float nl = neg_scaled(lse[t]);
-      const float ng = -gt;
-      const int64_t tl = yt - vocab_start - c0;  // target column inside this group, if any
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (c0 + i < V_valid) d[i] = (i == tl) ? dz_target(zv[i], nl, gt) : dz_other(zv[i], nl, ng);
+    for (int u = 0; u < DZS_UNROLL; ++u) {
+      const int c0 = base + u * DZS_THREADS * 8;
+      if (c0 < n_valid) {
+        const float4* zp = reinterpret_cast<const float4*>(zr + c0);
+        zv[u][0] = zp[0];
+        zv[u][1] = zp[1];
+      }
     }
-    uint4 w;
-    w.x = pack_bf16x2(d[0], d[1]);
-    w.y = pack_bf16x2(d[2], d[3]);
-    w.z = pack_bf16x2(d[4], d[5]);
-    w.w = pack_bf16x2(d[6], d[7]);
-    *reinterpret_cast<uint4*>(dz + static_cast<size_t>(t) * dz_ld + c0) = w;
+#pragma unroll
+    for (int u = 0; u < DZS_UNROLL; ++u) {
+      const int c0 = base + u * DZS_THREADS * 8;
+      if (c0 >= Vd) break;
+      float d[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) d[i] = 0.f;
+      if (c0 < n_valid) {
+        const float v8[8] = {zv[u][0].x, zv[u][0].y, zv[u][0].z, zv[u][0].w,
+                             zv[u][1].x, zv[u][1].y, zv[u][1].z, zv[u][1].w};
+        const int64_t tl = tcol - c0;  // target column inside this group, if any
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (c0 + i < n_valid) d[i] = (i == tl) ? dz_target(v8[i], nl, gt) : dz_other(v8[i], nl, ng);
+      }
+      uint4 w;
+      w.x = pack_bf16x2(d[0], d[1]);
+      w.y = pack_bf16x2(d[2], d[3]);
+      w.z = pack_bf16x2(d[4], d[5]);
+      w.w = pack_bf16x2(d[6], d[7]);
+      *reinterpret_cast<uint4*>(dr + c0) = w;
+    }
   }
 }
 
-// dz from saved bf16 probabilities: p = e(z - m) (bf16) x e(m - lse), m the row's
-// running max recorded per 64-column chunk; eight consecutive columns per thread.
-__global__ void dz_from_probs_kernel(const uint16_t* pb, const float* pm, int64_t ld,
-                                     const int64_t* y, const float* lse, const float* g, int T,
-                                     int Vd, int V_valid, int vocab_start, int V_true,
-                                     uint16_t* dz, int64_t dz_ld, int32_t* err_flag) {
-  const int64_t groups = static_cast<int64_t>(Vd / 8);
-  const int64_t total = static_cast<int64_t>(T) * groups;
-  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int t = static_cast<int>(idx / groups);
-    const int c0 = static_cast<int>(idx - static_cast<int64_t>(t) * groups) * 8;
-    const int64_t yt = y[t];
-    const bool yvalid = yt >= 0 && yt < V_true;
-    if (!yvalid && c0 == 0 && err_flag) atomicOr(err_flag, RLK_FLAG_BAD_TARGET);
-    float d[8];
+// dz from saved bf16 probabilities: p = e(z - m) (bf16) x e(m - lse), m the row's running
+// max recorded per 64-column chunk. Same block-per-row structure as dz_from_logits_kernel.
+__global__ void __launch_bounds__(DZS_THREADS)
+    dz_from_probs_kernel(const uint16_t* __restrict__ pb, const float* __restrict__ pm, int64_t ld,
+                         const int64_t* __restrict__ y, const float* __restrict__ lse,
+                         const float* __restrict__ g, int Vd, int V_valid, int vocab_start,
+                         int V_true, uint16_t* __restrict__ dz, int64_t dz_ld, int32_t* err_flag) {
+  const int t = blockIdx.x;
+  const int64_t yt = y[t];
+  const bool yvalid = yt >= 0 && yt < V_true;
+  if (!yvalid && threadIdx.x == 0 && err_flag) atomicOr(err_flag, RLK_FLAG_BAD_TARGET);
+  const float gt = g[t];
+  const float nls = neg_scaled(lse[t]);
+  const int64_t tcol = yt - vocab_start;
+  const uint16_t* pr = pb + static_cast<size_t>(t) * ld;
+  const float* pmr = pm + static_cast<size_t>(t) * (ld / 64);
+  uint16_t* dr = dz + static_cast<size_t>(t) * dz_ld;
+  const int n_valid = yvalid ? V_valid : 0;
+  for (int base = threadIdx.x * 8; base < Vd; base += DZS_THREADS * 8 * DZS_UNROLL) {
+    uint4 raw[DZS_UNROLL];
+    float mx[DZS_UNROLL];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) d[i] = 0.f;
-    if (yvalid && c0 < V_valid) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(pb + static_cast<size_t>(t) * ld + c0);
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-      const float gt = g[t];
-      const float scale = exp_shifted(pm[static_cast<size_t>(t) * (ld / 64) + c0 / 64], neg_scaled(lse[t]));
-      const int64_t tl = yt - vocab_start - c0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t bits = (i & 1) ? (w[i >> 1] & 0xFFFF0000u) : (w[i >> 1] << 16);
-        const float p = __fmul_rn(__uint_as_float(bits), scale);
-        if (c0 + i < V_valid) d[i] = (i == tl) ? __fmul_rn(gt, __fsub_rn(1.f, p)) : __fmul_rn(-gt, p);
+    for (int u = 0; u < DZS_UNROLL; ++u) {
+      const int c0 = base + u * DZS_THREADS * 8;
+      if (c0 < n_valid) {
+        raw[u] = *reinterpret_cast<const uint4*>(pr + c0);
+        mx[u] = pmr[c0 / 64];
       }
     }
-    uint4 o;
-    o.x = pack_bf16x2(d[0], d[1]);
-    o.y = pack_bf16x2(d[2], d[3]);
-    o.z = pack_bf16x2(d[4], d[5]);
-    o.w = pack_bf16x2(d[6], d[7]);
-    *reinterpret_cast<uint4*>(dz + static_cast<size_t>(t) * dz_ld + c0) = o;
+#pragma unroll
+    for (int u = 0; u < DZS_UNROLL; ++u) {
+      const int c0 = base + u * DZS_THREADS * 8;
+      if (c0 >= Vd) break;
+      float d[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) d[i] = 0.f;
+      if (c0 < n_valid) {
+        const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+        const float scale = exp_shifted(mx[u], nls);
+        const int64_t tl = tcol - c0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t bits = (i & 1) ? (w[i >> 1] & 0xFFFF0000u) : (w[i >> 1] << 16);
+          const float p = __fmul_rn(__uint_as_float(bits), scale);
+          if (c0 + i < n_valid) d[i] = (i == tl) ? __fmul_rn(gt, __fsub_rn(1.f, p)) : __fmul_rn(-gt, p);
+        }
+      }
+      uint4 o;
+      o.x = pack_bf16x2(d[0], d[1]);
+      o.y = pack_bf16x2(d[2], d[3]);
+      o.z = pack_bf16x2(d[4], d[5]);
+      o.w = pack_bf16x2(d[6], d[7]);
+      *reinterpret_cast<uint4*>(dr + c0) = o;
+    }
   }
 }
 
@@ -677,24 +714,17 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
   // 1. dz (bf16) workspace: from saved probabilities, saved logits, or recomputed z tiles
   if (p_saved) {
     const int64_t V_valid = std::max<int64_t>(0, std::min<int64_t>(V_true - vocab_start, V_local));
-    const int64_t total = T * (Vd / 8);
-    const int threads = 256;
-    const int64_t blocks = std::min<int64_t>(ceil_div(total, threads), 1 << 20);
-    dz_from_probs_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(
+    dz_from_probs_kernel<<<static_cast<unsigned>(T), DZS_THREADS, 0, s>>>(  // one block per row
         static_cast<const uint16_t*>(p_saved),
         reinterpret_cast<const float*>(static_cast<const char*>(p_saved) + saved_probs_offset(T, V_local)),
-        Vd, y, lse, g, static_cast<int>(T), static_cast<int>(Vd), static_cast<int>(V_valid),
+        Vd, y, lse, g, static_cast<int>(Vd), static_cast<int>(V_valid),
         static_cast<int>(vocab_start), static_cast<int>(V_true), dz, Vd, err_flag);
     if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
   } else if (z_saved) {
     const int64_t V_valid = std::max<int64_t>(0, std::min<int64_t>(V_true - vocab_start, V_local));
-    const int64_t total = T * (Vd / 8);
-    const int threads = 256;
-    const int64_t blocks = std::min<int64_t>(ceil_div(total, threads), 1 << 20);
-    dz_from_logits_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(
-        z_saved, Vd, y, lse, g, static_cast<int>(T), static_cast<int>(Vd),
-        static_cast<int>(V_valid), static_cast<int>(vocab_start), static_cast<int>(V_true), dz, Vd,
-        err_flag);
+    dz_from_logits_kernel<<<static_cast<unsigned>(T), DZS_THREADS, 0, s>>>(  // one block per row
+        z_saved, Vd, y, lse, g, static_cast<int>(Vd), static_cast<int>(V_valid),
+        static_cast<int>(vocab_start), static_cast<int>(V_true), dz, Vd, err_flag);
     if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
   } else {
     const int eb = f8 ? 1 : 2;  // element bytes of the logit operands
