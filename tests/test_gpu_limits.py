@@ -66,6 +66,27 @@ def test_largest_hidden(rlk, oracle_mod):
                       what="dW")
 
 
+def test_token_reduction_longer_than_one_accumulation_chunk(rlk, oracle_mod):
+    # dW sums over the tokens; past 65536 tokens the tensor-core accumulator is restarted
+    # and the chunk sums are folded in ascending order into the fp32 dW itself (the path
+    # that keeps plain stores). 65536 + 300 tokens: one full chunk and a ragged one.
+    T, H, V, Vt = 65536 + 300, 64, 512, 500
+    d = workloads.make_inputs(workloads.Workload("longT", T=T, H=H, V=V, V_true=Vt, seed=6))
+    h, W, y, g = dev_bf16(d["h"]), dev_bf16(d["W"]), dev(d["y"]), dev(d["g"])
+    logp, lse = rlk.linear_logp_fwd(h, W, y, Vt)
+    dH, dW = rlk.linear_logp_bwd(h, W, y, lse, g, Vt)
+    torch.cuda.synchronize()
+    ref_logp, ref_lse = oracle_mod.forward(d["h"], d["W"], d["y"], Vt)
+    assert_logp_close(logp.cpu().numpy(), ref_logp)
+    g64 = d["g"].astype(np.float64)
+    ref_dW = oracle_mod.backward_dw(d["h"], d["W"], d["y"], g64, ref_lse, Vt)
+    assert_grad_close(dW.cpu().numpy(), ref_dW, what="dW")
+    assert torch.count_nonzero(dW[Vt:]).item() == 0
+    rows = workloads.sample_rows(T, 64, seed=7)
+    ref_dH = oracle_mod.backward_dh(d["h"], d["W"], d["y"], g64, Vt, rows=rows)
+    assert_grad_close(host_bf16_to_f64(dH[torch.from_numpy(rows).cuda()]), ref_dH, what="dH rows")
+
+
 def test_one_past_the_limits_is_rejected(rlk):
     lib = rlk.lib()
     import ctypes
