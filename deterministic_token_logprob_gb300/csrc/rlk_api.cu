@@ -106,6 +106,9 @@ __device__ __forceinline__ Triple shfl_xor_triple(const Triple& x, int d) {
 // walk over all slots.
 
 __global__ void leaf_tree_kernel(const TreeArgs a) {
+  // Launched as a programmatic dependent of the forward tile kernel: wait until that grid
+  // has completed and its leaf statistics are visible (returns at once otherwise).
+  griddep_wait();
   const int t = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= a.T) return;  // warp-uniform
@@ -601,7 +604,18 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
   ta.lse = lse;
   ta.err_flag = err_flag;
   const int warps_per_block = 8;  // one warp per token
-  leaf_tree_kernel<<<static_cast<unsigned>(ceil_div(T, warps_per_block)), 32 * warps_per_block, 0, s>>>(ta);
+  // Programmatic stream serialization: the tree kernel's launch overlaps the tail of the
+  // tile kernel (it waits for the tile kernel's completion inside, griddep_wait).
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(T, warps_per_block)), 1, 1);
+  cfg.blockDim = dim3(32 * warps_per_block, 1, 1);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, leaf_tree_kernel, ta) != cudaSuccess) return RLK_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
 }
 

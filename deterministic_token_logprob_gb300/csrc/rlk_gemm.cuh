@@ -844,6 +844,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   cluster_sync();  // both CTAs' barriers exist before any cross-CTA arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The kernel that follows in the stream (the forward's leaf-tree merge) may be scheduled
+  // now; it waits for this grid's completion before it reads anything.
+  griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) producer_loop<MODE>(maps, a, smem, full, empty, ring, c);

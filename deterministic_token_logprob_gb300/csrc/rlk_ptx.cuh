@@ -45,6 +45,18 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched after this one with the programmatic
+// stream-serialization attribute may be scheduled once every CTA of this grid has
+// executed launch_dependents (or exited); the dependent's griddep_wait() then returns only
+// after this grid has completed and its memory operations are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
