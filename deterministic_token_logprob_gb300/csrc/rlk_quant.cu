@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
   uint32_t mag = 0;
   bool bad = false;
   if (vec) {
+#pragma unroll 4
     for (int64_t c = static_cast<int64_t>(lane) * 16; c < cols; c += 32 * 16) {
       const uint4 u0 = *reinterpret_cast<const uint4*>(xr + c);
       const uint4 u1 = *reinterpret_cast<const uint4*>(xr + c + 8);
@@ -77,8 +78,9 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
   const float p1 = ldexpf(1.f, s1), p2 = ldexpf(1.f, -e - s1);
   if (lane == 0) scale[r] = ldexpf(1.f, e);
 
-  // pass 2: codes
+  // pass 2: codes (the row was just read: these loads mostly hit in L1 / L2)
   if (vec) {
+#pragma unroll 4
     for (int64_t c = static_cast<int64_t>(lane) * 16; c < cols; c += 32 * 16) {
       const uint4 u0 = *reinterpret_cast<const uint4*>(xr + c);
       const uint4 u1 = *reinterpret_cast<const uint4*>(xr + c + 8);

@@ -55,14 +55,18 @@ def _quant_rows(rng, rows, cols):
     return workloads.bf16_bits(x.astype(np.float32))
 
 
-@pytest.mark.parametrize("rows,cols", [(37, 64), (5, 24), (9, 4096), (3, 8), (1, 16), (70, 2064)])
+# 4096 and 2048 columns take the one-pass kernel (rows held in registers), the others the
+# general two-pass kernel (vector and scalar paths)
+@pytest.mark.parametrize("rows,cols", [(37, 64), (5, 24), (9, 4096), (11, 2048), (3, 8), (1, 16),
+                                       (70, 2064)])
 def test_quantize_bit_exact(rlk, oracle_mod, rows, cols):
     rng = np.random.default_rng(rows * 1000 + cols)
     _assert_quant_equal(rlk, oracle_mod, _quant_rows(rng, rows, cols))
 
 
-def test_quantize_non_finite_row_is_flagged(rlk):
-    x = np.ones((4, 32), np.float32)
+@pytest.mark.parametrize("cols", [32, 2048, 4096])
+def test_quantize_non_finite_row_is_flagged(rlk, cols):
+    x = np.ones((4, cols), np.float32)
     x[2, 5] = np.inf
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     q, s = rlk.quantize_rows_e4m3(dev_bf16(workloads.bf16_bits(x)), err_flag=err)
