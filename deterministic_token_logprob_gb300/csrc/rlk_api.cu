@@ -752,8 +752,8 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
     a.vocab_start = static_cast<int32_t>(vocab_start);
     a.V_true = static_cast<int32_t>(V_true);
     a.n_pm = n_pm;
-    if ((Vd / BN) * static_cast<int64_t>(n_pm) > INT32_MAX) return RLK_ERR_UNSUPPORTED;
-    a.n_items = static_cast<int32_t>(Vd / BN) * n_pm;
+    a.n_vt = static_cast<int32_t>(Vd / BN);
+    a.n_items = static_cast<int32_t>(ceil_div(a.n_vt, DZ_UNIT)) * n_pm;  // checked above
     a.n_kb = static_cast<int32_t>(ceil_div(H, f8 ? BK8 : BK));
     if (f8) {
       a.a_scale = f8->h_scale;

@@ -63,7 +63,7 @@ struct Operands {
 };
 
 // Work-item order of the forward and dz kernels: items are (vocab unit, token pair-tile)
-// pairs, vocab unit = leaf (forward) or 256-column tile (dz). Token pair-tiles are taken in
+// pairs, vocab unit = leaf (forward) or DZ_UNIT 256-column tiles (dz). Token pair-tiles are taken in
 // groups of TOKEN_GROUP; inside a group the items run vocab-unit-major, so the clusters
 // working at one time touch at most TOKEN_GROUP token tiles of h (32 MiB of bf16 h at
 // H = 4096), and W is streamed once per group. Measured at T = 8192 (GB300, items handed
@@ -96,6 +96,10 @@ __device__ __forceinline__ int item_tiles(const GemmArgs& a, int item) {
     const int col0 = (a.leaf0 + leaf_local) * LEAF;
     const int end = min(col0 + LEAF, a.V_true);
     return (end - col0 + BN - 1) / BN;
+  } else if constexpr (is_dz<MODE>) {
+    int vu, pm;
+    item_unit_pm(a, a.n_items / a.n_pm, item, vu, pm);
+    return min(DZ_UNIT, a.n_vt - vu * DZ_UNIT);
   } else {
     return 1;
   }
@@ -118,10 +122,10 @@ __device__ __forceinline__ void tile_origin(const GemmArgs& a, int item, int j, 
     m0 = pm * PAIR_M;
     n0 = (a.leaf0 + leaf_local) * LEAF + j * BN - a.vocab_start;
   } else if constexpr (is_dz<MODE>) {
-    int vt, pm;
-    item_unit_pm(a, a.n_items / a.n_pm, item, vt, pm);
+    int vu, pm;
+    item_unit_pm(a, a.n_items / a.n_pm, item, vu, pm);
     m0 = pm * PAIR_M;
-    n0 = vt * BN;
+    n0 = (vu * DZ_UNIT + j) * BN;
   } else {
     // dH / dW: output column tiles in groups of COL_GROUP, row-tile-major inside a group
     const int g0 = (item / (COL_GROUP * a.n_mt)) * COL_GROUP;  // first column tile of the group
@@ -648,8 +652,9 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
           }
         }
       } else if constexpr (is_dz<MODE>) {
-        const int gc0 = a.vocab_start + n0;
-        const int vcols = max(0, min(min(BN, a.V_true - gc0), a.V_local - n0));
+        const int nt0 = n0 + j * BN;  // local column of this tile
+        const int gc0 = a.vocab_start + nt0;
+        const int vcols = max(0, min(min(BN, a.V_true - gc0), a.V_local - nt0));
         const int tl = (yvalid && yt >= gc0 && yt < static_cast<int64_t>(gc0) + vcols)
                            ? static_cast<int>(yt - gc0) : -1;
         const float ng = -g_t;
@@ -657,7 +662,7 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
         for (int ch = 0; ch < BN; ch += 64) {
           float v[64];
           tmem_ld64(taddr + ch, v);
-          if constexpr (is_e4m3<MODE>) apply_row_col_scales(v, s_row, a.b_scale, n0 + ch, a.V_local);
+          if constexpr (is_e4m3<MODE>) apply_row_col_scales(v, s_row, a.b_scale, nt0 + ch, a.V_local);
           const int tli = tl - ch;
           float d_target = 0.f;
           const bool any_target = __any_sync(0xffffffffu, tli >= 0 && tli < 64);
@@ -683,7 +688,7 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
             const uint32_t buf = stage_begin(stg, lane);
 #pragma unroll
             for (int q = 0; q < 8; ++q) stage_chunk(buf, lane, q, pack8_bf16(v + 8 * q));
-            stage_store(stg, buf, lane, out_map, n0 + ch, m0 + row0_off, pol_out);
+            stage_store(stg, buf, lane, out_map, nt0 + ch, m0 + row0_off, pol_out);
           }
         }
       } else {
