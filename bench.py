@@ -407,13 +407,15 @@ def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int)
     }
 
     if rank == 0 and world == 1 and not args.quick:
+        # the end-to-end step first, right after the device-timed loop, so that both run in
+        # the same thermal and power state; the other legs follow
+        line["e2e"] = e2e(rlk, torch, path, wr, d, device, args, gpu_uuid(torch, device))
         if w.name == "qwen3_8b":  # legs defined on the Qwen3-8B weight
             line["fwd_only"] = fwd_only(rlk, torch, W_bits, path, device, args, peak)
             line["saved_logits"] = saved_logits_leg(rlk, torch, path, wr, device, args, peak, peak_sus)
             line["saved_probs_bf16"] = saved_probs_leg(rlk, torch, path, wr, device, args, peak)
             line["small_T_forward"] = small_t_leg(rlk, torch, path, device, peaks)
             line["fp8_e4m3"] = fp8_leg(rlk, torch, path, wr, device, args, peak)
-        line["e2e"] = e2e(rlk, torch, path, wr, d, device, args)
         rate, cores, sample = oracle_sample_rate(wr, d)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
@@ -664,7 +666,7 @@ def fwd_only(rlk, torch, W_bits, path, device, args, peak):
             "frac_of_burst": tf / peak, "steps": K}
 
 
-def e2e(rlk, torch, path, w, d, device, args):
+def e2e(rlk, torch, path, w, d, device, args, gpu_id=None):
     """Same step through the public API from pinned host buffers: every step copies
     its inputs (h, y, g) host -> device, runs the C-ABI calls and copies its result
     (logp) device -> host, all inside the timed region. The weight W is model state
@@ -710,16 +712,24 @@ def e2e(rlk, torch, path, w, d, device, args):
     run(max(3, args.warmup))
     torch.cuda.synchronize(device)
     K = args.steps
+    sampler = ClockSampler(gpu_id) if gpu_id else None
+    if sampler:
+        sampler.wait_running()
+        sampler.mark_start()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(compute)
     run(K)
     b.record(compute)
     torch.cuda.synchronize(device)
+    if sampler:
+        sampler.mark_end()
+    clocks = sampler.stop() if sampler else None
     path.h, path.y, path.g = sets[0]
     ms = a.elapsed_time(b) / K
     return {"value": w.T / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-            "pipeline": "inputs of step k+1 copied on a second stream while step k computes"}
+            "pipeline": "inputs of step k+1 copied on a second stream while step k computes",
+            "clocks": clocks}
 
 
 def run_case(args):
