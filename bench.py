@@ -489,19 +489,25 @@ def small_t_leg(rlk, torch, path, device, peaks):
         ws = torch.empty(rlk.fwd_workspace_bytes(T, H, V), dtype=torch.uint8, device=device)
         for _ in range(5):
             rlk.linear_logp_fwd(h, W, y, Vt, out=(logp, lse), workspace=ws)
-        n = 20
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(device)
-        a.record()
-        for _ in range(n):
-            rlk.linear_logp_fwd(h, W, y, Vt, out=(logp, lse), workspace=ws)
-        b.record()
-        torch.cuda.synchronize(device)
-        ms = a.elapsed_time(b) / n
+        # five repeats of 20 back-to-back calls, the median repeat reported: right after the
+        # heavy legs the power controller is still settling, which moved single repeats by ~10 %
+        n, reps = 20, []
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(device)
+            a.record()
+            for _ in range(n):
+                rlk.linear_logp_fwd(h, W, y, Vt, out=(logp, lse), workspace=ws)
+            b.record()
+            torch.cuda.synchronize(device)
+            reps.append(a.elapsed_time(b) / n)
+        ms = statistics.median(reps)
         nbytes = V * H * 2 + T * H * 2 + 3 * 4 * T * -(-V // 1024)
         gbs = nbytes / (ms / 1e3) / 1e9
-        out[str(T)] = {"us_per_call": ms * 1e3, "algorithmic_GBps": gbs, "frac_of_hbm": gbs / hbm}
-    out["note"] = "W and L2 are not flushed between calls; W (1.24 GB) exceeds L2 on its own"
+        out[str(T)] = {"us_per_call": ms * 1e3, "us_per_call_best": min(reps) * 1e3,
+                       "algorithmic_GBps": gbs, "frac_of_hbm": gbs / hbm}
+    out["note"] = ("W and L2 are not flushed between calls; W (1.24 GB) exceeds L2 on its own; "
+                   "median of 5 repeats of 20 calls")
     return out
 
 
