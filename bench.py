@@ -391,12 +391,14 @@ def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int)
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_dict(w, world),
         "gpu_launches": K * path.launches_per_step(),
+        # the forward kernel is timed inside the back-to-back, power-capped fwd+bwd loop,
+        # so its denominator is the sustained bf16 figure; the burst fraction is kept beside it
         "roofline": {"bound": "tensor", "kernel": "forward tile GEMM + online statistics",
-                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak,
+                     "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
+                     "frac": achieved / peak_sus,
                      "traffic": fwd_traffic_per_launch() if w.name == "qwen3_8b" else None,
-                     "peak_source": f"{peaks_src} bf16 burst",
-                     "frac_of_sustained": achieved / peak_sus,
+                     "peak_source": f"{peaks_src} bf16 sustained (kernel timed inside the step loop)",
+                     "frac_of_burst": achieved / peak,
                      "algorithmic_flops_per_launch": flops_fwd, "avg_launch_ms": fwd_avg},
         "step_roofline": {"flops_counted": step_flops, "roofline_ms": roofline_ms,
                           "frac_of_burst": roofline_ms / ms_per_step,
