@@ -63,10 +63,10 @@ struct Operands {
 };
 
 // Work-item order of the forward and dz kernels: items are (vocab unit, token pair-tile)
-// pairs, vocab unit = leaf (forward) or DZ_UNIT 256-column tiles (dz). Token pair-tiles are taken in
-// groups of TOKEN_GROUP; inside a group the items run vocab-unit-major, so the clusters
-// working at one time touch at most TOKEN_GROUP token tiles of h (32 MiB of bf16 h at
-// H = 4096), and W is streamed once per group. Measured at T = 8192 (GB300, items handed
+// pairs, vocab unit = leaf (forward) or DZ_UNIT 256-column tiles (dz). Token pair-tiles
+// are taken in groups of TOKEN_GROUP; inside a group the items run vocab-unit-major, so
+// the clusters working at one time touch at most TOKEN_GROUP token tiles of h (32 MiB of
+// bf16 h at H = 4096), and W is streamed once per group. Measured at T = 8192 (GB300, items handed
 // out in order): groups of 16 read 3.4 GB (forward) and 2.6 GB (dz) from DRAM; one group of
 // all 32 token tiles read 9.4 / 7.7 GB (64 MiB of h does not stay in L2) and made the
 // power-capped fwd+bwd step 3 % slower. The order changes only which cluster computes a
