@@ -202,6 +202,36 @@ def test_sharded_forward_is_bitwise_unsharded(rlk, oracle_mod, S, V, Vt):
     assert_grad_close(host_bf16_to_f64(dH_s), ref_dH, what="sharded dH")
 
 
+def test_targets_on_tile_leaf_shard_and_vocab_boundaries(rlk, oracle_mod):
+    # targets at the first and last column of 256-column tiles, 1024-column leaves, the last
+    # valid column and the columns on both sides of every shard boundary of an 8-way split
+    H, V, Vt = 192, 24576, 24000
+    bounds = rlk.shard_bounds(V, Vt, 8)
+    ys = {0, 1, 255, 256, 1023, 1024, 1025, Vt - 2, Vt - 1}
+    for a, _ in bounds[1:]:
+        ys |= {a - 1, a, a + 1}
+    y_np = np.array(sorted(ys), dtype=np.int64)
+    T = y_np.shape[0]
+    d = _inputs(T, H, V, Vt, seed=91)
+    h, W, y, g = dev_bf16(d["h"]), dev_bf16(d["W"]), dev(y_np), dev(d["g"])
+    logp, lse = rlk.linear_logp_fwd(h, W, y, Vt)
+    dH, dW = rlk.linear_logp_bwd(h, W, y, lse, g, Vt)
+    torch.cuda.synchronize()
+    ref_logp, ref_lse = oracle_mod.forward(d["h"], d["W"], y_np, Vt)
+    assert_logp_close(logp.cpu().numpy(), ref_logp)
+    g64 = d["g"].astype(np.float64)
+    assert_grad_close(host_bf16_to_f64(dH), oracle_mod.backward_dh(d["h"], d["W"], y_np, g64, Vt), what="dH")
+    assert_grad_close(dW.cpu().numpy(), oracle_mod.backward_dw(d["h"], d["W"], y_np, g64, ref_lse, Vt),
+                      what="dW")
+    # exactly one shard owns each target; the merged shards give the unsharded bits
+    parts = torch.stack([rlk.linear_logp_fwd(h, W[a:a + n], y, Vt, vocab_start=a, partial=True)
+                         for a, n in bounds])
+    owners = torch.isfinite(parts[:, :, 2]).sum(dim=0)
+    assert torch.all(owners == 1)
+    slogp, slse = rlk.lse_merge(parts)
+    assert torch.equal(slogp, logp) and torch.equal(slse, lse)
+
+
 def test_lse_merge_against_oracle(rlk, oracle_mod):
     rng = np.random.default_rng(3)
     for S in (1, 2, 4, 8):
