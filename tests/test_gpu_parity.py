@@ -87,10 +87,22 @@ def test_large_logit_range(rlk, oracle_mod):
     assert_logp_close(logp.cpu().numpy(), ref_logp)
     assert_logp_close(lse.cpu().numpy(), ref_lse)
     g64 = g.astype(np.float64)
-    assert_grad_close(host_bf16_to_f64(dH), oracle_mod.backward_dh(hb, Wb, d["y"], g64, Vt), what="dH")
-    assert_grad_close(dW.cpu().numpy(), oracle_mod.backward_dw(hb, Wb, d["y"], g64, ref_lse, Vt),
-                      what="dW")
+    ref_dH = oracle_mod.backward_dh(hb, Wb, d["y"], g64, Vt)
+    assert_grad_close(host_bf16_to_f64(dH), ref_dH, what="dH")
+    ref_dW = oracle_mod.backward_dw(hb, Wb, d["y"], g64, ref_lse, Vt)
+    assert_grad_close(dW.cpu().numpy(), ref_dW, what="dW")
     assert torch.count_nonzero(dH[::7]).item() == 0
+    # the saved-logits pair gives the same bits; the saved bf16 probabilities stay within
+    # tolerance (each probability is stored relative to its 64-column running maximum)
+    (logp2, lse2), z = rlk.linear_logp_fwd_save(h, W, y, Vt)
+    dH2, dW2 = rlk.linear_logp_bwd_saved(h, W, y, lse, gd, z, Vt)
+    assert torch.equal(logp2, logp) and torch.equal(lse2, lse)
+    assert torch.equal(dH2, dH) and torch.equal(dW2, dW)
+    (logp3, lse3), pbuf = rlk.linear_logp_fwd_save_probs(h, W, y, Vt)
+    dH3, dW3 = rlk.linear_logp_bwd_saved_probs(h, W, y, lse, gd, pbuf, Vt)
+    assert torch.equal(logp3, logp) and torch.equal(lse3, lse)
+    assert_grad_close(host_bf16_to_f64(dH3), ref_dH, what="dH (saved probs)")
+    assert_grad_close(dW3.cpu().numpy(), ref_dW, what="dW (saved probs)")
 
 
 def test_fp32_dH_partial_matches(rlk, oracle_mod):
