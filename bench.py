@@ -38,29 +38,64 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_BYTES = 129 * 1024 * 1024
 
 
-def fwd_traffic_per_launch():
-    """dram read + write bytes of one forward launch on the Qwen3-8B workload, from the
-    committed ncu summary, or None if the kernel sources changed since it was taken."""
-    import hashlib
-    path = os.path.join(ROOT, "profiles", "traffic_fwd_qwen3_8b.md")
-    if not os.path.exists(path):
-        return None
-    vals = {}
-    with open(path) as f:
-        for line in f:
-            if "=" in line and line.startswith("    "):
-                k, v = line.strip().split("=", 1)
-                vals[k.strip()] = v.strip()
-    try:
-        h = hashlib.sha256()
-        for name in vals["sources"].split():
-            with open(os.path.join(ROOT, "deterministic_token_logprob_gb300", "csrc", name), "rb") as f:
-                h.update(f.read())
-        if h.hexdigest() != vals["sources_sha256"]:
-            return None
-        return int(vals["traffic_bytes_per_launch"])
-    except (KeyError, OSError, ValueError):
-        return None
+# DRAM traffic per launch of each tile kernel, from one ncu capture of the full-size step
+# (`--record-traffic` writes it; bench reads it back only while the library's sources
+# still hash to the value recorded with it).
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_qwen3_8b.json")
+STAGE_OF_MODE = {0: "fwd", 1: "dz", 2: "dH", 3: "dW"}
+
+
+def record_traffic(csv_path: str, command: str, out_path: str = TRAFFIC_FILE):
+    """Parse an ncu --csv log of dram__bytes_read.sum / dram__bytes_write.sum over tile-kernel
+    launches and write the per-launch averages with the current sources hash."""
+    import csv
+    import re
+    from deterministic_token_logprob_gb300 import build as libbuild
+    acc = {}
+    with open(csv_path, newline="") as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    for row in csv.DictReader(lines):
+        m = re.search(r"gemm_kernel<\(?(?:int\))?(\d+)>", row.get("Kernel Name", ""))
+        metric = row.get("Metric Name", "")
+        if not m or int(m.group(1)) not in STAGE_OF_MODE or not metric.startswith("dram__bytes_"):
+            continue
+        scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}.get(row.get("Metric Unit", "byte"))
+        if scale is None:
+            raise ValueError(f"unknown unit {row.get('Metric Unit')}")
+        val = float(row["Metric Value"].replace(",", "")) * scale
+        e = acc.setdefault(STAGE_OF_MODE[int(m.group(1))], {"ids": set(), "read": 0.0, "write": 0.0})
+        e["ids"].add(row["ID"])
+        e["read" if "read" in metric else "write"] += val
+    kernels = {}
+    for stage, e in acc.items():
+        n = len(e["ids"])
+        kernels[stage] = {"launches": n, "dram_bytes_read_per_launch": e["read"] / n,
+                          "dram_bytes_write_per_launch": e["write"] / n,
+                          "traffic_bytes_per_launch": (e["read"] + e["write"]) / n}
+    rec = {"workload": "qwen3_8b fwd+bwd T=8192 H=4096 V=151936 V_true=151669",
+           "metrics": "dram__bytes_read.sum + dram__bytes_write.sum (ncu, 1 pass per launch)",
+           "command": command, "library_sources_sha256": libbuild.sources_sha256(),
+           "kernels": kernels}
+    with open(out_path, "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    return rec
+
+
+def traffic_per_launch(stage: str):
+    """(bytes, note): the recorded DRAM traffic of one launch of `stage`'s kernel on the
+    Qwen3-8B workload, or (None, why) when there is no record for the current sources."""
+    from deterministic_token_logprob_gb300 import build as libbuild
+    if not os.path.exists(TRAFFIC_FILE):
+        return None, "no traffic record"
+    with open(TRAFFIC_FILE) as f:
+        rec = json.load(f)
+    if rec.get("library_sources_sha256") != libbuild.sources_sha256():
+        return None, "traffic record predates the current library sources"
+    k = rec.get("kernels", {}).get(stage)
+    if not k:
+        return None, f"no {stage} launch in the traffic record"
+    return k["traffic_bytes_per_launch"], f"ncu capture: {rec.get('command')}"
 
 
 def load_peaks():
@@ -263,6 +298,33 @@ class Path:
         n = len(self.shards)
         return (2 * n + 1 + 3 * n + 1) if self.w.shards else 5
 
+    def staged_calls(self):
+        """The step as a list of (stage, call): the forward, then the backward as its three
+        stages (rlk_linear_logp_bwd_stages: the launches of one rlk_linear_logp_bwd call, one
+        call each), so that each stage can be timed inside the step."""
+        rlk, w = self.rlk, self.w
+        DZ, DH, DW = rlk.RLK_BWD_DZ, rlk.RLK_BWD_DH, rlk.RLK_BWD_DW
+        if not w.shards:
+            def bwd(stage):
+                return lambda: rlk.linear_logp_bwd(self.h, self.W, self.y, self.lse, self.g, w.V_true,
+                                                   out=(self.dH, self.dW), workspace=self.bws,
+                                                   stages=stage)
+            return [("fwd", self.forward), ("dz", bwd(DZ)), ("dH", bwd(DH)), ("dW", bwd(DW))]
+        calls = []
+        for i, (a, n) in enumerate(self.shards):
+            calls.append(("fwd", lambda a=a, n=n, i=i: rlk.linear_logp_fwd(
+                self.h, self.W[a:a + n], self.y, w.V_true, vocab_start=a, partial=True,
+                out=(self.parts[i],), workspace=self.fws)))
+        calls.append(("merge", lambda: rlk.lse_merge(self.parts, out=(self.logp, self.lse))))
+        for i, (a, n) in enumerate(self.shards):
+            for name, stage in (("dz", DZ), ("dH", DH), ("dW", DW)):
+                calls.append((name, lambda a=a, n=n, i=i, stage=stage: rlk.linear_logp_bwd(
+                    self.h, self.W[a:a + n], self.y, self.lse, self.g, w.V_true, vocab_start=a,
+                    dH_fp32_partial=True, out=(self.dH_parts[i], self.dW[a:a + n]),
+                    workspace=self.bws, stages=stage)))
+        calls.append(("sum", lambda: rlk.shard_sum_bf16(self.dH_parts, out=self.dH)))
+        return calls
+
     def forward(self):
         rlk, w = self.rlk, self.w
         if not w.shards:
@@ -340,73 +402,75 @@ def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int)
         if world > 1:
             torch.distributed.barrier()
 
+    first_legs = {}
+    if rank == 0 and world == 1 and not args.quick:
+        # the short, HBM-bound and launch-bound legs first, before any power-capped loop has
+        # heated the GPU, each with its own clock record
+        if w.name == "qwen3_8b":
+            first_legs["small_T_forward"] = small_t_leg(rlk, torch, path, device, peaks,
+                                                        gpu_uuid(torch, device))
+        first_legs["tiny"] = tiny_leg(rlk, torch, device, args, gpu_uuid(torch, device))
+
+    calls = path.staged_calls()
     for _ in range(args.warmup):
-        path.forward()
-        path.backward()
+        for _, fn in calls:
+            fn()
     torch.cuda.synchronize(device)
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     sampler = ClockSampler(gpu_uuid(torch, device)) if rank == 0 else None
     if sampler:
         sampler.wait_running()
     barrier()
     torch.cuda.synchronize(device)
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
     if sampler:
         sampler.mark_start()
-    t_start.record(stream)
-    for i in range(K):
-        ev[i][0].record(stream)
-        path.forward()
-        ev[i][1].record(stream)
-        path.backward()
-        ev[i][2].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize(device)
+    res = timed_steps(torch, stream, calls, K)
     if sampler:
         sampler.mark_end()
     barrier()
     clocks = sampler.stop() if sampler else None
-    total_ms = t_start.elapsed_time(t_end)
-    fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
-    bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
-    step_ms = sorted(a.elapsed_time(c) for a, _, c in ev)
-    total_ms = max_over_ranks(total_ms, world, device)
+    total_ms = max_over_ranks(res["total_ms"], world, device)
     ms_per_step = total_ms / K
     tokens_per_s = job_tokens_per_s(w.T, world, K, total_ms)
 
-    flops_fwd = 2.0 * w.T * w.H * w.V_true
-    fwd_avg = statistics.mean(fwd_ms)
-    achieved = flops_fwd / (fwd_avg / 1e3) / 1e12
+    flops_gemm = 2.0 * w.T * w.H * w.V_true   # one GEMM-equivalent: each of fwd, dz, dH, dW
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    step_flops = 3.0 * flops_fwd
+    step_flops = 3.0 * flops_gemm
     roofline_ms = step_flops / (peak * 1e12) * 1e3
+    per_kernel = per_kernel_roofline(res["stage_ms"], flops_gemm, peak, peak_sus)
+    dominant = max(per_kernel, key=lambda k: per_kernel[k]["ms"])
+    dk = per_kernel[dominant]
+    traffic, traffic_note = (traffic_per_launch(dominant) if w.name == "qwen3_8b"
+                             else (None, "traffic is recorded for the qwen3_8b workload only"))
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_dict(w, world),
         "gpu_launches": K * path.launches_per_step(),
-        # the forward kernel is timed inside the back-to-back, power-capped fwd+bwd loop,
-        # so its denominator is the sustained bf16 figure; the burst fraction is kept beside it
-        "roofline": {"bound": "tensor", "kernel": "forward tile GEMM + online statistics",
-                     "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
-                     "frac": achieved / peak_sus,
-                     "traffic": fwd_traffic_per_launch() if w.name == "qwen3_8b" else None,
+        # the dominant (slowest) GEMM kernel of the step, timed with CUDA events around its call
+        # inside the back-to-back, power-capped loop: its denominator is the sustained bf16
+        # figure; the burst fraction is kept beside it
+        "roofline": {"bound": "tensor", "kernel": STAGE_LABEL[dominant],
+                     "achieved": dk["tflops"], "peak": peak_sus, "unit": "TFLOP/s",
+                     "frac": dk["frac_of_sustained"], "traffic": traffic,
+                     "traffic_source": traffic_note,
                      "peak_source": f"{peaks_src} bf16 sustained (kernel timed inside the step loop)",
-                     "frac_of_burst": achieved / peak,
-                     "algorithmic_flops_per_launch": flops_fwd, "avg_launch_ms": fwd_avg},
+                     "frac_of_burst": dk["frac_of_burst"],
+                     "algorithmic_flops_per_launch": flops_gemm, "avg_launch_ms": dk["ms"],
+                     "per_kernel": per_kernel},
         "step_roofline": {"flops_counted": step_flops, "roofline_ms": roofline_ms,
                           "frac_of_burst": roofline_ms / ms_per_step,
                           "frac_of_sustained": (step_flops / (peak_sus * 1e12) * 1e3) / ms_per_step,
-                          "fwd_ms": fwd_avg, "bwd_ms": statistics.mean(bwd_ms),
-                          "step_ms_median": statistics.median(step_ms), "step_ms_best": step_ms[0]},
+                          "stage_ms": res["stage_ms"],
+                          "step_ms_median": statistics.median(res["step_ms"]),
+                          "step_ms_best": min(res["step_ms"]),
+                          "note": "step = forward call + the backward's three stages (one call each)"},
         "clocks": clocks,
     }
+    line.update(first_legs)
 
     if rank == 0 and world == 1 and not args.quick:
         # the end-to-end step first, right after the device-timed loop, so that both run in
@@ -416,13 +480,122 @@ def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int)
             line["fwd_only"] = fwd_only(rlk, torch, W_bits, path, device, args, peak)
             line["saved_logits"] = saved_logits_leg(rlk, torch, path, wr, device, args, peak, peak_sus)
             line["saved_probs_bf16"] = saved_probs_leg(rlk, torch, path, wr, device, args, peak)
-            line["small_T_forward"] = small_t_leg(rlk, torch, path, device, peaks)
             line["fp8_e4m3"] = fp8_leg(rlk, torch, path, wr, device, args, peak)
+            del path, calls
+            torch.cuda.empty_cache()
+            line["qwen3_30b_tp2"] = sharded_leg(rlk, torch, device, args, peak, peak_sus,
+                                                gpu_uuid(torch, device))
         rate, cores, sample = oracle_sample_rate(wr, d)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+STAGE_LABEL = {"fwd": "forward tile GEMM + online statistics (call incl. leaf tree)",
+               "dz": "dz: logits recompute + softmax gradient (MODE_DZ)",
+               "dH": "dH = dz W (MODE_DH)", "dW": "dW = dz^T h (MODE_DW)"}
+
+
+def timed_steps(torch, stream, calls, K):
+    """K back-to-back steps of `calls` ([(stage, fn)]) with a CUDA event on `stream` before
+    every call and after the last: total ms, per-step ms and mean ms per step of each stage
+    (a stage's calls summed within a step)."""
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(K):
+        for j, (_, fn) in enumerate(calls):
+            evs[i][j].record(stream)
+            fn()
+        evs[i][-1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    stage_ms = {}
+    for i in range(K):
+        for j, (name, _) in enumerate(calls):
+            stage_ms[name] = stage_ms.get(name, 0.0) + evs[i][j].elapsed_time(evs[i][j + 1]) / K
+    return {"total_ms": t_start.elapsed_time(t_end),
+            "step_ms": [e[0].elapsed_time(e[-1]) for e in evs], "stage_ms": stage_ms}
+
+
+def per_kernel_roofline(stage_ms, flops_gemm, peak, peak_sus):
+    """Achieved TFLOP/s of each GEMM stage (one GEMM-equivalent, 2 T H V_true FLOP, per call)
+    against the measured sustained and burst bf16 peaks."""
+    out = {}
+    for k in ("fwd", "dz", "dH", "dW"):
+        if k in stage_ms:
+            tf = flops_gemm / (stage_ms[k] / 1e3) / 1e12
+            out[k] = {"ms": stage_ms[k], "tflops": tf, "frac_of_sustained": tf / peak_sus,
+                      "frac_of_burst": tf / peak}
+    return out
+
+
+def sharded_leg(rlk, torch, device, args, peak, peak_sus, gpu_id):
+    """The Qwen3-30B-A3B-shaped step with two vocab shards emulated on this GPU (T = 16384,
+    H = 2048; shards [0, 77824) and [77824, 151936)): per shard the forward statistics, then
+    rlk_lse_merge; per shard dz, the fp32 dH partial and its dW rows, then rlk_shard_sum_bf16."""
+    w = workloads.QWEN3_30B_TP2
+    d = workloads.make_inputs(w)
+    path = Path(rlk, torch, w, d, device)
+    calls = path.staged_calls()
+    for _ in range(max(3, args.warmup)):
+        for _, fn in calls:
+            fn()
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(gpu_id) if gpu_id else None
+    if sampler:
+        sampler.wait_running()
+        sampler.mark_start()
+    res = timed_steps(torch, torch.cuda.current_stream(device), calls, args.steps)
+    if sampler:
+        sampler.mark_end()
+    clocks = sampler.stop() if sampler else None
+    ms = res["total_ms"] / args.steps
+    flops_gemm = 2.0 * w.T * w.H * w.V_true
+    step_flops = 3.0 * flops_gemm
+    out = {"workload": config_dict(w, 1)["workload"], "tokens_per_s": w.T / (ms / 1e3),
+           "ms_per_step": ms, "steps": args.steps,
+           "frac_of_burst": step_flops / (peak * 1e12) / (ms / 1e3),
+           "frac_of_sustained": step_flops / (peak_sus * 1e12) / (ms / 1e3),
+           "gpu_launches_per_step": path.launches_per_step(),
+           "per_kernel": per_kernel_roofline(res["stage_ms"], flops_gemm, peak, peak_sus),
+           "stage_ms": res["stage_ms"], "clocks": clocks,
+           "shards": [list(x) for x in w.shards]}
+    del path
+    torch.cuda.empty_cache()
+    return out
+
+
+def tiny_leg(rlk, torch, device, args, gpu_id):
+    """The tiny workload (T = 64, H = 256, V = V_true = 4096) fwd+bwd: launch-bound."""
+    w = workloads.TINY
+    d = workloads.make_inputs(w)
+    path = Path(rlk, torch, w, d, device)
+    K = max(50, args.steps)
+    for _ in range(max(3, args.warmup)):
+        path.forward()
+        path.backward()
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(gpu_id) if gpu_id else None
+    if sampler:
+        sampler.wait_running()
+        sampler.mark_start()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(K):
+        path.forward()
+        path.backward()
+    b.record()
+    torch.cuda.synchronize(device)
+    if sampler:
+        sampler.mark_end()
+    clocks = sampler.stop() if sampler else None
+    ms = a.elapsed_time(b) / K
+    return {"workload": config_dict(w, 1)["workload"], "tokens_per_s": w.T / (ms / 1e3),
+            "us_per_step": ms * 1e3, "steps": K, "gpu_launches_per_step": path.launches_per_step(),
+            "bound": "launch latency (5 kernels of a few microseconds each)", "clocks": clocks}
 
 
 def saved_logits_leg(rlk, torch, path, w, device, args, peak, peak_sus):
@@ -474,15 +647,20 @@ def _peaks_hbm():
     return float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
 
 
-def small_t_leg(rlk, torch, path, device, peaks):
+def small_t_leg(rlk, torch, path, device, peaks, gpu_id=None):
     """Forward latency at small T (the batch-invariance workload's batch sizes) on the
     Qwen3-8B weight: these calls stream W once and are HBM-bound; reported as achieved
-    GB/s of algorithmic bytes (W + h read, statistics written) against measured HBM."""
+    GB/s of algorithmic bytes (W + h read, statistics written) against measured HBM.
+    Runs before the power-capped legs, with its own clock record."""
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     W = path.W
     V, H = W.shape
     Vt = path.w.V_true
     out = {}
+    sampler = ClockSampler(gpu_id) if gpu_id else None
+    if sampler:
+        sampler.wait_running()
+        sampler.mark_start()
     for T in (1, 7, 128, 1000):
         h = torch.from_numpy(workloads.make_h(T, H, 9).view(np.int16)).view(torch.bfloat16).to(device)
         y = torch.from_numpy(workloads.make_y(T, Vt, 9)).to(device)
@@ -508,8 +686,11 @@ def small_t_leg(rlk, torch, path, device, peaks):
         gbs = nbytes / (ms / 1e3) / 1e9
         out[str(T)] = {"us_per_call": ms * 1e3, "us_per_call_best": min(reps) * 1e3,
                        "algorithmic_GBps": gbs, "frac_of_hbm": gbs / hbm}
+    if sampler:
+        sampler.mark_end()
+    out["clocks"] = sampler.stop() if sampler else None
     out["note"] = ("W and L2 are not flushed between calls; W (1.24 GB) exceeds L2 on its own; "
-                   "median of 5 repeats of 20 calls")
+                   "median of 5 repeats of 20 calls; run first, before the power-capped legs")
     return out
 
 
@@ -737,6 +918,8 @@ def e2e(rlk, torch, path, w, d, device, args, gpu_id=None):
     return {"value": w.T / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms,
             "pipeline": "inputs of step k+1 copied on a second stream while step k computes",
+            "d2h": ("logp only; dH and dW stay on the device, where the model's backward and the "
+                    "optimizer consume them"),
             "clocks": clocks}
 
 
@@ -810,7 +993,14 @@ def main():
     ap.add_argument("--tokens", type=int, default=1024, help="tokens for --case")
     ap.add_argument("--vocab", type=int, default=0,
                     help="vocab rows for --case (default 151936; V_true = V - 267)")
+    ap.add_argument("--record-traffic", metavar="NCU_CSV", default=None,
+                    help="write the per-launch DRAM traffic of an ncu --csv capture of the "
+                         "qwen3_8b step to profiles/traffic_qwen3_8b.json and exit")
+    ap.add_argument("--traffic-command", default="", help="the command that made NCU_CSV")
     args = ap.parse_args()
+    if args.record_traffic:
+        print(json.dumps(record_traffic(args.record_traffic, args.traffic_command), indent=1))
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.case:

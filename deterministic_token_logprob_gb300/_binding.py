@@ -25,6 +25,10 @@ RLK_FLAG_BAD_TARGET = 1
 RLK_FLAG_TIMEOUT = 2
 RLK_FLAG_NONFINITE = 4
 
+RLK_BWD_DZ = 1
+RLK_BWD_DH = 2
+RLK_BWD_DW = 4
+
 LEAF_WIDTH = 1024
 MAX_SHARDS = 8
 
@@ -66,6 +70,9 @@ def _load():
         lib.rlk_linear_logp_bwd.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, P, I32, P, P,
                                             P, SZ, P]
         lib.rlk_linear_logp_bwd.restype = ctypes.c_int
+        lib.rlk_linear_logp_bwd_stages.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, P, I32, P,
+                                                   I32, P, P, SZ, P]
+        lib.rlk_linear_logp_bwd_stages.restype = ctypes.c_int
         lib.rlk_saved_logits_bytes.argtypes = [I64, I64]
         lib.rlk_saved_logits_bytes.restype = SZ
         lib.rlk_linear_logp_fwd_save.argtypes = [P, P, P, I64, I64, I64, I64, I64, P, P, P, P, SZ,
@@ -223,8 +230,13 @@ def linear_logp_bwd(h: torch.Tensor, W: torch.Tensor, y: torch.Tensor, lse: torc
                     dH_fp32_partial: bool = False, want_dH: bool = True, want_dW: bool = True,
                     out: Optional[Tuple[Optional[torch.Tensor], Optional[torch.Tensor]]] = None,
                     err_flag: Optional[torch.Tensor] = None,
-                    workspace: Optional[torch.Tensor] = None, stream=None):
-    """rlk_linear_logp_bwd -> (dH, dW); dH bf16 [T, H] (fp32 if dH_fp32_partial), dW fp32 [V_local, H]."""
+                    workspace: Optional[torch.Tensor] = None, stages: Optional[int] = None,
+                    stream=None):
+    """rlk_linear_logp_bwd -> (dH, dW); dH bf16 [T, H] (fp32 if dH_fp32_partial), dW fp32 [V_local, H].
+
+    stages (an OR of RLK_BWD_DZ / RLK_BWD_DH / RLK_BWD_DW) calls rlk_linear_logp_bwd_stages
+    instead: only those stages run, and the dz they share lives in `workspace`, which the
+    caller then passes, unchanged, to the calls of the later stages."""
     _need(h, "h", torch.bfloat16, 2)
     _need(W, "W", torch.bfloat16, 2)
     _need(y, "y", torch.int64, 1)
@@ -247,13 +259,23 @@ def linear_logp_bwd(h: torch.Tensor, W: torch.Tensor, y: torch.Tensor, lse: torc
         _need(dW, "dW", torch.float32, 2)
     if err_flag is not None:
         _need(err_flag, "err_flag", torch.int32, 1)
+    if stages is not None and workspace is None:
+        raise ValueError("stages need a caller-owned workspace (it carries dz between the calls)")
     ws = _workspace(bwd_workspace_bytes(T, H, V_local), dev, workspace)
     nbytes = 0 if ws is None else ws.numel() * ws.element_size()
-    st = _load().rlk_linear_logp_bwd(_ptr(h), _ptr(W), _ptr(y), _ptr(lse), _ptr(g), T, H, V_local,
-                                     int(vocab_start), int(V_true), _ptr(dH),
-                                     1 if dH_fp32_partial else 0, _ptr(dW), _ptr(err_flag),
-                                     _ptr(ws), nbytes, _stream_handle(stream))
-    _check("rlk_linear_logp_bwd", st)
+    if stages is None:
+        st = _load().rlk_linear_logp_bwd(_ptr(h), _ptr(W), _ptr(y), _ptr(lse), _ptr(g), T, H,
+                                         V_local, int(vocab_start), int(V_true), _ptr(dH),
+                                         1 if dH_fp32_partial else 0, _ptr(dW), _ptr(err_flag),
+                                         _ptr(ws), nbytes, _stream_handle(stream))
+        _check("rlk_linear_logp_bwd", st)
+    else:
+        st = _load().rlk_linear_logp_bwd_stages(_ptr(h), _ptr(W), _ptr(y), _ptr(lse), _ptr(g), T, H,
+                                                V_local, int(vocab_start), int(V_true), _ptr(dH),
+                                                1 if dH_fp32_partial else 0, _ptr(dW), int(stages),
+                                                _ptr(err_flag), _ptr(ws), nbytes,
+                                                _stream_handle(stream))
+        _check("rlk_linear_logp_bwd_stages", st)
     return dH, dW
 
 

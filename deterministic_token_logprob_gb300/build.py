@@ -40,11 +40,18 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _stamp(extra) -> str:
+def sources_sha256() -> str:
+    """SHA-256 over every source file the library is compiled from (in a fixed order): two
+    builds with the same value run the same kernels."""
     h = hashlib.sha256()
     for p in [os.path.join(CSRC, s) for s in SOURCES] + HEADERS:
         with open(p, "rb") as f:
             h.update(f.read())
+    return h.hexdigest()
+
+
+def _stamp(extra) -> str:
+    h = hashlib.sha256(sources_sha256().encode())
     h.update(" ".join(ARCH + FLAGS + list(extra)).encode())
     return h.hexdigest()
 

@@ -697,7 +697,8 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
                     int64_t vocab_start, int64_t V_true, void* dH, int32_t dH_fp32_partial,
                     float* dW, int32_t* err_flag, void* workspace, size_t workspace_bytes,
                     void* stream, const void* p_saved = nullptr, const void* hq = nullptr,
-                    const void* Wq = nullptr, const Fp8In* f8 = nullptr) {
+                    const void* Wq = nullptr, const Fp8In* f8 = nullptr,
+                    int32_t stages = RLK_BWD_DZ | RLK_BWD_DH | RLK_BWD_DW) {
   rlk_status st = common_checks(h, W, y, T, H, V_local, vocab_start, V_true);
   if (st != RLK_OK) return st;
   if (f8) {  // straight-through: dz from the E4M3 logits, dH / dW with the bf16 operands
@@ -726,7 +727,9 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
                                               bwd_run_bytes(T, H, V_local));  // dz, dH, dW
 
   // 1. dz (bf16) workspace: from saved probabilities, saved logits, or recomputed z tiles
-  if (p_saved) {
+  if (!(stages & RLK_BWD_DZ)) {
+    // the workspace already holds this shard's dz (rlk_linear_logp_bwd_stages)
+  } else if (p_saved) {
     const int64_t V_valid = std::max<int64_t>(0, std::min<int64_t>(V_true - vocab_start, V_local));
     dz_from_probs_kernel<<<static_cast<unsigned>(T), DZS_THREADS, 0, s>>>(  // one block per row
         static_cast<const uint16_t*>(p_saved),
@@ -772,7 +775,7 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
   }
 
   // 2. dH = dz W over this shard's valid columns
-  if (dH) {
+  if (dH && (stages & RLK_BWD_DH)) {
     const int64_t V_valid = std::max<int64_t>(0, std::min<int64_t>(V_true - vocab_start, V_local));
     const size_t elem = dH_fp32_partial ? 4 : 2;
     if (V_valid == 0) {
@@ -809,7 +812,7 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
   }
 
   // 3. dW = dz^T h (rows at or above V_true come out exactly zero: their dz is zero)
-  if (dW) {
+  if (dW && (stages & RLK_BWD_DW)) {
     TileMaps maps{};
     GemmArgs a;
     if (!encode_mn(&maps.a, dz, Vd, T, &a.a_mn_wide)) return RLK_ERR_CUDA;
@@ -850,6 +853,20 @@ rlk_status rlk_linear_logp_bwd(const void* h, const void* W, const int64_t* y, c
                                void* workspace, size_t workspace_bytes, void* stream) {
   return bwd_impl(h, W, y, lse, g, nullptr, T, H, V_local, vocab_start, V_true, dH,
                   dH_fp32_partial, dW, err_flag, workspace, workspace_bytes, stream);
+}
+
+rlk_status rlk_linear_logp_bwd_stages(const void* h, const void* W, const int64_t* y,
+                                      const float* lse, const float* g, int64_t T, int64_t H,
+                                      int64_t V_local, int64_t vocab_start, int64_t V_true,
+                                      void* dH, int32_t dH_fp32_partial, float* dW,
+                                      int32_t stages, int32_t* err_flag, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  constexpr int32_t all = RLK_BWD_DZ | RLK_BWD_DH | RLK_BWD_DW;
+  if (stages == 0 || (stages & ~all) != 0) return RLK_ERR_INVALID_ARG;
+  if (((stages & RLK_BWD_DH) && !dH) || ((stages & RLK_BWD_DW) && !dW)) return RLK_ERR_INVALID_ARG;
+  return bwd_impl(h, W, y, lse, g, nullptr, T, H, V_local, vocab_start, V_true, dH,
+                  dH_fp32_partial, dW, err_flag, workspace, workspace_bytes, stream, nullptr,
+                  nullptr, nullptr, nullptr, stages);
 }
 
 rlk_status rlk_linear_logp_bwd_saved(const void* h, const void* W, const int64_t* y,

@@ -6,7 +6,9 @@
 // loaded on a GPU and held by every GPU that loads the library until the process
 // exits. Host code cannot use the array's name as a device address (on the host it
 // names a shadow variable), so the device address is looked up once per device
-// with cudaGetSymbolAddress and cached.
+// with cudaGetSymbolAddress and cached for the life of the process (after a
+// cudaDeviceReset the module is loaded anew and the cached address would be stale:
+// calling this entry point after a reset is not supported).
 //
 // All calls on a device share this one array and it keeps the previous call's
 // contents. The one part that must start at zero, the tile kernel's work-item

@@ -195,6 +195,37 @@ RLK_API rlk_status rlk_linear_logp_bwd(const void* h, const void* W, const int64
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The same backward, launched in separate stages. The backward's three products
+ * meet in its workspace ("tiled logits / dlogits and linear-gradient work ... with
+ * a controlled workspace", "Announcing RL-Kernel for vime", section "Why the Fused
+ * Path Wins", fourth reason): the dz tiles are written there once and read by both
+ * gradient products. `stages` is a nonzero OR of
+ *   RLK_BWD_DZ  recompute the logits and write dz into the workspace
+ *   RLK_BWD_DH  dH = dz W from the dz the workspace holds (dH must not be NULL)
+ *   RLK_BWD_DW  dW = dz^T h from the dz the workspace holds (dW must not be NULL)
+ * and every other argument is as in rlk_linear_logp_bwd. A stage launches exactly
+ * the kernel, with exactly the arguments, that rlk_linear_logp_bwd launches for it,
+ * so stages run one call at a time in the order DZ, DH, DW with one workspace give
+ * the bits of a single rlk_linear_logp_bwd call. The workspace must stay untouched
+ * from the DZ call until the last call that reads its dz. Each stage has its own
+ * work-item counter in the workspace and only RLK_BWD_DH uses its fp32 running sum,
+ * so once the DZ stage has completed, the DH and DW stages may run on two streams
+ * at the same time. Uses: pipeline schedules that need the input gradient dH at once
+ * and defer the weight gradient dW; timing each stage on its own.
+ */
+#define RLK_BWD_DZ 1
+#define RLK_BWD_DH 2
+#define RLK_BWD_DW 4
+
+RLK_API rlk_status rlk_linear_logp_bwd_stages(const void* h, const void* W, const int64_t* y,
+                                              const float* lse, const float* g, int64_t T,
+                                              int64_t H, int64_t V_local, int64_t vocab_start,
+                                              int64_t V_true, void* dH, int32_t dH_fp32_partial,
+                                              float* dW, int32_t stages, int32_t* err_flag,
+                                              void* workspace, size_t workspace_bytes,
+                                              void* stream);
+
+/*
  * Saved-logits variant of the pair above: the forward also stores the fp32
  * logits it computed and the backward forms dz from them instead of recomputing
  * the logits GEMM (the "save-logits fused-tile full-gradient path" named in
@@ -344,7 +375,9 @@ RLK_API rlk_status rlk_linear_logp_bwd_fp8(const void* h, const void* W, const v
  * rlk_linear_logp_fwd_workspace(T, H, V_local) exceeds that size is rejected with
  * RLK_ERR_WORKSPACE before anything runs (e.g. at most 9383 tokens for a 151936-row
  * W). The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture. All calls on a
+ * device current) and keeps it for the life of the process; make that first call
+ * before any stream capture. Calling it after cudaDeviceReset on that device is not
+ * supported (the array may then live at another address). All calls on a
  * device share the array: calls that can overlap on the GPU (different streams with
  * no ordering between them) race and give wrong results.
  */

@@ -140,6 +140,24 @@ def test_backward_argument_errors(lib):
     assert bwd(lib, ws=None) == WORKSPACE
 
 
+def test_backward_stages_argument_errors(lib):
+    def st(stages, dH=FAKE, dW=FAKE, T=4, ws_bytes=1 << 30):
+        return lib.rlk_linear_logp_bwd_stages(FAKE, FAKE, FAKE, FAKE, FAKE, T, 64, 4096, 0, 4096, dH,
+                                              0, dW, stages, None, FAKE, ws_bytes, None)
+    DZ, DH, DW = 1, 2, 4
+    assert st(0) == INVALID                   # no stage
+    assert st(8) == INVALID                   # unknown bit
+    assert st(DZ | 16) == INVALID
+    assert st(DH, dH=None) == INVALID         # a selected output may not be missing
+    assert st(DW, dW=None) == INVALID
+    assert st(DZ | DH | DW, dH=None) == INVALID
+    assert st(DZ, dH=None, dW=None, T=0) == OK
+    assert st(DH, T=0) == OK
+    need = lib.rlk_linear_logp_bwd_workspace(4, 64, 4096)
+    assert st(DZ, ws_bytes=need - 1) == WORKSPACE
+    assert st(DW, ws_bytes=need - 1) == WORKSPACE
+
+
 def test_merge_and_sum_argument_errors(lib):
     assert lib.rlk_lse_merge(FAKE, 3, 10, FAKE, FAKE, None) == UNSUPPORTED
     assert lib.rlk_lse_merge(None, 2, 10, FAKE, FAKE, None) == INVALID

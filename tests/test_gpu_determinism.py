@@ -84,6 +84,49 @@ def test_two_calls_running_at_once_on_two_streams(rlk):
                 assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("shape", [(700, 512, 9000, 8999), (300, 256, 70000, 69000)])
+def test_backward_stages_match_one_call(rlk, shape):
+    # The backward launched stage by stage (dz, then dH, then dW, sharing one workspace) gives
+    # the bits of one rlk_linear_logp_bwd call; so do dH and dW launched on two streams at once
+    # after dz. The second shape's dH reduces over more than one 65536-column chunk (fp32
+    # running sum in the workspace).
+    T, H, V, Vt = shape
+    w = workloads.Workload("stages", T=T, H=H, V=V, V_true=Vt, seed=33)
+    d = workloads.make_inputs(w)
+    h, W, y, g = dev_bf16(d["h"]), dev_bf16(d["W"]), dev(d["y"]), dev(d["g"])
+    _, lse = rlk.linear_logp_fwd(h, W, y, Vt)
+    for partial in (False, True):
+        ref_dH, ref_dW = rlk.linear_logp_bwd(h, W, y, lse, g, Vt, dH_fp32_partial=partial)
+        ws = torch.empty(rlk.bwd_workspace_bytes(T, H, V), dtype=torch.uint8, device="cuda")
+        dH = torch.full_like(ref_dH, float("nan"))
+        dW = torch.full_like(ref_dW, float("nan"))
+        out = (dH, dW)
+        rlk.linear_logp_bwd(h, W, y, lse, g, Vt, dH_fp32_partial=partial, out=out, workspace=ws,
+                            stages=rlk.RLK_BWD_DZ)
+        rlk.linear_logp_bwd(h, W, y, lse, g, Vt, dH_fp32_partial=partial, out=out, workspace=ws,
+                            stages=rlk.RLK_BWD_DH)
+        rlk.linear_logp_bwd(h, W, y, lse, g, Vt, dH_fp32_partial=partial, out=out, workspace=ws,
+                            stages=rlk.RLK_BWD_DW)
+        torch.cuda.synchronize()
+        assert torch.equal(dH, ref_dH) and torch.equal(dW, ref_dW)
+        # dH and dW at the same time on two streams, both after the dz stage
+        dH.fill_(float("nan"))
+        dW.fill_(float("nan"))
+        rlk.linear_logp_bwd(h, W, y, lse, g, Vt, dH_fp32_partial=partial, out=out, workspace=ws,
+                            stages=rlk.RLK_BWD_DZ)
+        dz_done = torch.cuda.Event()
+        dz_done.record()
+        side = torch.cuda.Stream()
+        side.wait_event(dz_done)
+        with torch.cuda.stream(side):
+            rlk.linear_logp_bwd(h, W, y, lse, g, Vt, dH_fp32_partial=partial, out=out, workspace=ws,
+                                stages=rlk.RLK_BWD_DW, stream=side)
+        rlk.linear_logp_bwd(h, W, y, lse, g, Vt, dH_fp32_partial=partial, out=out, workspace=ws,
+                            stages=rlk.RLK_BWD_DH)
+        torch.cuda.synchronize()
+        assert torch.equal(dH, ref_dH) and torch.equal(dW, ref_dW)
+
+
 def _invariance(rlk, H, V, Vt, W_bits, W_dev, Ts, oracle_mod=None, check_dH=True):
     th, ty = workloads.invariance_targets(0, H=H, V_true=Vt)
     n = th.shape[0]
