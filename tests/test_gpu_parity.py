@@ -330,3 +330,32 @@ def test_saved_probs_path(rlk, oracle_mod, T, H, V, Vt):
         _, dWp = rlk.linear_logp_bwd_saved_probs(h, W[a:a + n], y, lse, g, pb, Vt, vocab_start=a,
                                                  want_dH=False)
         assert_grad_close(dWp.cpu().numpy(), ref_dW[a:a + n], what="shard dW (saved probs)")
+
+
+def test_dH_large_batch_sampled_rows_and_sub_batch(rlk, oracle_mod):
+    # dH at T = 8192, H = 2048 (32 row tiles x 8 column tiles: several waves of work items over
+    # the resident CTA pairs): sampled rows against the oracle, and every row of a 512-row
+    # sub-batch (2 x 8 items, all in the first wave) bit for bit against the same rows of the
+    # full batch, in bf16 and as the fp32 shard partial.
+    T, H, V, Vt = 8192, 2048, 20480, 20000
+    d = _inputs(T, H, V, Vt, seed=88)
+    h, W, y, g = dev_bf16(d["h"]), dev_bf16(d["W"]), dev(d["y"]), dev(d["g"])
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    logp, lse = rlk.linear_logp_fwd(h, W, y, Vt, err_flag=err)
+    dH, _ = rlk.linear_logp_bwd(h, W, y, lse, g, Vt, want_dW=False, err_flag=err)
+    dHp, _ = rlk.linear_logp_bwd(h, W, y, lse, g, Vt, want_dW=False, dH_fp32_partial=True)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rows = np.concatenate([np.arange(0, T, 331), np.arange(4860, 4870), [T - 1]])
+    g64 = d["g"].astype(np.float64)
+    ref = oracle_mod.backward_dh(d["h"], d["W"], d["y"], g64, Vt, rows=rows)
+    assert_grad_close(host_bf16_to_f64(dH)[rows], ref, what="dH")
+    assert_grad_close(dHp.cpu().numpy()[rows], ref, what="dH fp32")
+    lo = 4608
+    sub = slice(lo, lo + 512)
+    hs, ys, gs, ls = h[sub].contiguous(), y[sub].contiguous(), g[sub].contiguous(), lse[sub].contiguous()
+    dHs, _ = rlk.linear_logp_bwd(hs, W, ys, ls, gs, Vt, want_dW=False)
+    dHps, _ = rlk.linear_logp_bwd(hs, W, ys, ls, gs, Vt, want_dW=False, dH_fp32_partial=True)
+    torch.cuda.synchronize()
+    assert torch.equal(dHs, dH[sub])
+    assert torch.equal(dHps, dHp[sub])
