@@ -593,8 +593,29 @@ def tiny_leg(rlk, torch, device, args, gpu_id):
         sampler.mark_end()
     clocks = sampler.stop() if sampler else None
     ms = a.elapsed_time(b) / K
+    # the same step captured once in a CUDA graph and replayed: what remains is the kernels'
+    # own latency (prologue, one short tile pass, tail) without the host's launch overhead
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            path.forward()
+            path.backward()
+    torch.cuda.current_stream(device).wait_stream(side)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize(device)
+    a.record()
+    for _ in range(K):
+        graph.replay()
+    b.record()
+    torch.cuda.synchronize(device)
+    gms = a.elapsed_time(b) / K
+    del graph
     return {"workload": config_dict(w, 1)["workload"], "tokens_per_s": w.T / (ms / 1e3),
             "us_per_step": ms * 1e3, "steps": K, "gpu_launches_per_step": path.launches_per_step(),
+            "graph_replay": {"us_per_step": gms * 1e3, "tokens_per_s": w.T / (gms / 1e3)},
             "bound": "launch latency (5 kernels of a few microseconds each)", "clocks": clocks}
 
 
