@@ -52,7 +52,8 @@ def gather_stats(partial: torch.Tensor, group=None) -> torch.Tensor:
     S = dist.get_world_size(group)
     T = partial.shape[0]
     out = torch.empty((S * T,) + tuple(partial.shape[1:]), dtype=partial.dtype, device=partial.device)
-    dist.all_gather_into_tensor(out, partial.contiguous(), group=group)
+    if T:   # every rank holds the same tokens, so all ranks skip an empty batch together
+        dist.all_gather_into_tensor(out, partial.contiguous(), group=group)
     return out.view((S,) + tuple(partial.shape))
 
 
@@ -65,7 +66,9 @@ def sum_dH_partials(part: torch.Tensor, group=None,
         sum_fn = lambda parts: rlk.shard_sum_bf16(parts)  # noqa: E731
     S = dist.get_world_size(group)
     T, H = part.shape
-    rows = -(-T // S) if T else 0
+    if T == 0:  # the same on every rank: no rank enters the collectives
+        return torch.empty((0, H), dtype=torch.bfloat16, device=part.device)
+    rows = -(-T // S)
     if rows * S != T:   # pad to S equal row blocks; padding rows are summed and discarded
         padded = torch.zeros((rows * S, H), dtype=part.dtype, device=part.device)
         padded[:T] = part
@@ -73,8 +76,7 @@ def sum_dH_partials(part: torch.Tensor, group=None,
     blocks = torch.empty((S * rows, H), dtype=part.dtype, device=part.device)
     # rank r receives block r of every rank, in rank order
     dist.all_to_all_single(blocks, part.contiguous(), group=group)
-    mine = (sum_fn(blocks.view(S, rows, H)) if rows
-            else torch.empty((0, H), dtype=torch.bfloat16, device=part.device))
+    mine = sum_fn(blocks.view(S, rows, H))
     full = torch.empty((S * rows, H), dtype=mine.dtype, device=part.device)
     dist.all_gather_into_tensor(full, mine.contiguous(), group=group)
     return full[:T]

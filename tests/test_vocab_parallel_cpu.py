@@ -77,7 +77,10 @@ def _worker(rank, world, port, out):
             res[Tb] = (tuple(dh.shape), dh.dtype == torch.bfloat16,
                        torch.equal(dh.view(torch.int16), ref.view(torch.int16)),
                        dh.view(torch.int16).numpy().tobytes())
-        out[rank] = (fwd_bitwise, fwd_err, res)
+        # an empty batch: no collective is entered, empty results of the right shapes
+        empty = (tuple(vp.gather_stats(torch.empty((0, 3))).shape),
+                 tuple(vp.sum_dH_partials(torch.empty((0, 24)), sum_fn=_host_sum_bf16).shape))
+        out[rank] = (fwd_bitwise, fwd_err, res, empty)
     finally:
         dist.destroy_process_group()
 
@@ -91,7 +94,8 @@ def test_vocab_parallel_exchange_matches_single_process(world):
         res = dict(out)
     assert set(res) == set(range(world))
     for r in range(world):
-        fwd_bitwise, fwd_err, sums = res[r]
+        fwd_bitwise, fwd_err, sums, empty = res[r]
+        assert empty == ((world, 0, 3), (0, 24))
         assert fwd_bitwise, f"rank {r}: gathered statistics differ from the vocab-order stack"
         assert fwd_err < 1e-5, fwd_err     # fp32-rounded statistics merged in fp64
         for Tb, (shape, is_bf16, same, _) in sums.items():
