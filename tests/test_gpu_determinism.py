@@ -127,6 +127,27 @@ def test_backward_stages_match_one_call(rlk, shape):
         assert torch.equal(dH, ref_dH) and torch.equal(dW, ref_dW)
 
 
+def test_backward_stages_per_vocab_shard(rlk):
+    # the staged backward of each shard of a 2-way split (fp32 dH partials, the shard's dW
+    # rows) equals that shard's one-call backward bit for bit, as the sharded bench step uses it
+    T, H, V, Vt = 300, 256, 70000, 69000
+    w = workloads.Workload("stages_shard", T=T, H=H, V=V, V_true=Vt, seed=34)
+    d = workloads.make_inputs(w)
+    h, W, y, g = dev_bf16(d["h"]), dev_bf16(d["W"]), dev(d["y"]), dev(d["g"])
+    _, lse = rlk.linear_logp_fwd(h, W, y, Vt)
+    for a, n in rlk.shard_bounds(V, Vt, 2):
+        Ws = W[a:a + n]
+        ref_dH, ref_dW = rlk.linear_logp_bwd(h, Ws, y, lse, g, Vt, vocab_start=a, dH_fp32_partial=True)
+        ws = torch.empty(rlk.bwd_workspace_bytes(T, H, n), dtype=torch.uint8, device="cuda")
+        dH = torch.full_like(ref_dH, float("nan"))
+        dW = torch.full_like(ref_dW, float("nan"))
+        for st in (rlk.RLK_BWD_DZ, rlk.RLK_BWD_DH, rlk.RLK_BWD_DW):
+            rlk.linear_logp_bwd(h, Ws, y, lse, g, Vt, vocab_start=a, dH_fp32_partial=True,
+                                out=(dH, dW), workspace=ws, stages=st)
+        torch.cuda.synchronize()
+        assert torch.equal(dH, ref_dH) and torch.equal(dW, ref_dW), a
+
+
 def _invariance(rlk, H, V, Vt, W_bits, W_dev, Ts, oracle_mod=None, check_dH=True):
     th, ty = workloads.invariance_targets(0, H=H, V_true=Vt)
     n = th.shape[0]
