@@ -485,6 +485,7 @@ def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int)
             torch.cuda.empty_cache()
             line["qwen3_30b_tp2"] = sharded_leg(rlk, torch, device, args, peak, peak_sus,
                                                 gpu_uuid(torch, device))
+            line["qwen3_30b_tp2_rank_calls"] = tp2_rank_calls_leg(rlk, torch, device, args, peak)
         rate, cores, sample = oracle_sample_rate(wr, d)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
@@ -565,6 +566,51 @@ def sharded_leg(rlk, torch, device, args, peak, peak_sus, gpu_id):
            "shards": [list(x) for x in w.shards]}
     del path
     torch.cuda.empty_cache()
+    return out
+
+
+def tp2_rank_calls_leg(rlk, torch, device, args, peak):
+    """One rank's share of a two-way vocab split at the Qwen3-30B-A3B output layer (H = 2048,
+    shard [0, 77824) of V = 151936, V_true = 151669), for 796, 1820 and 6827 tokens per call:
+    the forward (the shard's statistics, then rlk_lse_merge with the other shard's) and the
+    forward + backward (plus dz, the fp32 dH partial and the shard's dW rows), each timed as
+    back-to-back calls with CUDA events. The exchange between ranks is not included."""
+    H, V, Vt = 2048, 151936, 151669
+    (a0, n0), (a1, n1) = rlk.shard_bounds(V, Vt, 2)
+    W = torch.from_numpy(workloads.make_W(n0, H, 3).view(np.int16)).view(torch.bfloat16).to(device)
+    out = {"shard": [a0, n0], "H": H, "V": V, "V_true": Vt}
+    for T in (796, 1820, 6827):
+        h = torch.from_numpy(workloads.make_h(T, H, T).view(np.int16)).view(torch.bfloat16).to(device)
+        y = torch.from_numpy(workloads.make_y(T, Vt, T)).to(device)
+        g = torch.from_numpy(np.random.default_rng(T).standard_normal(T).astype(np.float32)).to(device)
+        parts = torch.empty((2, T, 3), dtype=torch.float32, device=device)
+        parts[1, :, 0], parts[1, :, 1], parts[1, :, 2] = 5.0, 1000.0, float("-inf")  # other shard
+        logp = torch.empty(T, dtype=torch.float32, device=device)
+        lse = torch.empty(T, dtype=torch.float32, device=device)
+        dHp = torch.empty((T, H), dtype=torch.float32, device=device)
+        dW = torch.empty((n0, H), dtype=torch.float32, device=device)
+        fws = torch.empty(rlk.fwd_workspace_bytes(T, H, n0), dtype=torch.uint8, device=device)
+        bws = torch.empty(rlk.bwd_workspace_bytes(T, H, n0), dtype=torch.uint8, device=device)
+
+        def fwd():
+            rlk.linear_logp_fwd(h, W, y, Vt, vocab_start=a0, partial=True, out=(parts[0],),
+                                workspace=fws)
+            rlk.lse_merge(parts, out=(logp, lse))
+
+        def fwd_bwd():
+            fwd()
+            rlk.linear_logp_bwd(h, W, y, lse, g, Vt, vocab_start=a0, dH_fp32_partial=True,
+                                out=(dHp, dW), workspace=bws)
+
+        K = max(args.steps, 10)
+        f_ms, fb_ms = _time_calls(torch, device, fwd, K), _time_calls(torch, device, fwd_bwd, K)
+        flops = 2.0 * T * H * min(n0, Vt - a0)
+        out[str(T)] = {"fwd_ms": f_ms, "fwd_bwd_ms": fb_ms,
+                       "fwd_tflops": flops / (f_ms / 1e3) / 1e12,
+                       "fwd_bwd_tflops": 3 * flops / (fb_ms / 1e3) / 1e12,
+                       "fwd_frac_of_burst": flops / (f_ms / 1e3) / 1e12 / peak}
+    out["note"] = ("per-rank single-operator times; the backward's recompute GEMM is not "
+                   "counted in fwd_bwd_tflops (3 GEMM-equivalents credited, 4 run)")
     return out
 
 
