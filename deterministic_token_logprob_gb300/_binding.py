@@ -8,6 +8,7 @@ librlk.so is missing or a call fails, an exception is raised.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -24,6 +25,7 @@ RLK_ERR_CUDA = 4
 RLK_FLAG_BAD_TARGET = 1
 RLK_FLAG_TIMEOUT = 2
 RLK_FLAG_NONFINITE = 4
+RLK_FLAG_BOUNDS = 8
 
 RLK_BWD_DZ = 1
 RLK_BWD_DH = 2
@@ -57,56 +59,80 @@ def _load():
         if not os.path.exists(path):
             raise RuntimeError(f"librlk.so is not built ({path}); run "
                                "`python -m deterministic_token_logprob_gb300.build`")
-        lib = ctypes.CDLL(path)
-        P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
-        lib.rlk_linear_logp_fwd_workspace.argtypes = [I64, I64, I64]
-        lib.rlk_linear_logp_fwd_workspace.restype = SZ
-        lib.rlk_linear_logp_bwd_workspace.argtypes = [I64, I64, I64]
-        lib.rlk_linear_logp_bwd_workspace.restype = SZ
-        lib.rlk_linear_logp_fwd.argtypes = [P, P, P, I64, I64, I64, I64, I64, P, P, P, P, P, SZ, P]
-        lib.rlk_linear_logp_fwd.restype = ctypes.c_int
-        lib.rlk_lse_merge.argtypes = [P, I32, I64, P, P, P]
-        lib.rlk_lse_merge.restype = ctypes.c_int
-        lib.rlk_linear_logp_bwd.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, P, I32, P, P,
+        _lib = _declare(ctypes.CDLL(path))
+        return _lib
+
+
+def _declare(lib):
+    """Argument and result types of every entry point of include/rlk.h on a loaded library."""
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    lib.rlk_linear_logp_fwd_workspace.argtypes = [I64, I64, I64]
+    lib.rlk_linear_logp_fwd_workspace.restype = SZ
+    lib.rlk_linear_logp_bwd_workspace.argtypes = [I64, I64, I64]
+    lib.rlk_linear_logp_bwd_workspace.restype = SZ
+    lib.rlk_linear_logp_fwd.argtypes = [P, P, P, I64, I64, I64, I64, I64, P, P, P, P, P, SZ, P]
+    lib.rlk_linear_logp_fwd.restype = ctypes.c_int
+    lib.rlk_lse_merge.argtypes = [P, I32, I64, P, P, P]
+    lib.rlk_lse_merge.restype = ctypes.c_int
+    lib.rlk_linear_logp_bwd.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, P, I32, P, P,
+                                        P, SZ, P]
+    lib.rlk_linear_logp_bwd.restype = ctypes.c_int
+    lib.rlk_linear_logp_bwd_stages.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, P, I32, P,
+                                               I32, P, P, SZ, P]
+    lib.rlk_linear_logp_bwd_stages.restype = ctypes.c_int
+    lib.rlk_saved_logits_bytes.argtypes = [I64, I64]
+    lib.rlk_saved_logits_bytes.restype = SZ
+    lib.rlk_linear_logp_fwd_save.argtypes = [P, P, P, I64, I64, I64, I64, I64, P, P, P, P, SZ,
+                                             P, P, SZ, P]
+    lib.rlk_linear_logp_fwd_save.restype = ctypes.c_int
+    lib.rlk_linear_logp_bwd_saved.argtypes = [P, P, P, P, P, P, SZ, I64, I64, I64, I64, I64, P,
+                                              I32, P, P, P, SZ, P]
+    lib.rlk_linear_logp_bwd_saved.restype = ctypes.c_int
+    lib.rlk_saved_probs_bytes.argtypes = [I64, I64]
+    lib.rlk_saved_probs_bytes.restype = SZ
+    lib.rlk_linear_logp_fwd_save_probs.argtypes = [P, P, P, I64, I64, I64, I64, I64, P, P, P, P,
+                                                   SZ, P, P, SZ, P]
+    lib.rlk_linear_logp_fwd_save_probs.restype = ctypes.c_int
+    lib.rlk_linear_logp_bwd_saved_probs.argtypes = [P, P, P, P, P, P, SZ, I64, I64, I64, I64,
+                                                    I64, P, I32, P, P, P, SZ, P]
+    lib.rlk_linear_logp_bwd_saved_probs.restype = ctypes.c_int
+    lib.rlk_selftest_wait_timeout.argtypes = [P, P, P, I64, I64, I64, I64, P, P, P, P, SZ, P]
+    lib.rlk_selftest_wait_timeout.restype = ctypes.c_int
+    lib.rlk_shard_sum_bf16.argtypes = [P, I32, I64, P, P]
+    lib.rlk_shard_sum_bf16.restype = ctypes.c_int
+    lib.rlk_quantize_rows_e4m3.argtypes = [P, I64, I64, P, P, P, P]
+    lib.rlk_quantize_rows_e4m3.restype = ctypes.c_int
+    lib.rlk_linear_logp_fwd_fp8.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, P, P, P, P,
                                             P, SZ, P]
-        lib.rlk_linear_logp_bwd.restype = ctypes.c_int
-        lib.rlk_linear_logp_bwd_stages.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, P, I32, P,
-                                                   I32, P, P, SZ, P]
-        lib.rlk_linear_logp_bwd_stages.restype = ctypes.c_int
-        lib.rlk_saved_logits_bytes.argtypes = [I64, I64]
-        lib.rlk_saved_logits_bytes.restype = SZ
-        lib.rlk_linear_logp_fwd_save.argtypes = [P, P, P, I64, I64, I64, I64, I64, P, P, P, P, SZ,
-                                                 P, P, SZ, P]
-        lib.rlk_linear_logp_fwd_save.restype = ctypes.c_int
-        lib.rlk_linear_logp_bwd_saved.argtypes = [P, P, P, P, P, P, SZ, I64, I64, I64, I64, I64, P,
-                                                  I32, P, P, P, SZ, P]
-        lib.rlk_linear_logp_bwd_saved.restype = ctypes.c_int
-        lib.rlk_saved_probs_bytes.argtypes = [I64, I64]
-        lib.rlk_saved_probs_bytes.restype = SZ
-        lib.rlk_linear_logp_fwd_save_probs.argtypes = [P, P, P, I64, I64, I64, I64, I64, P, P, P, P,
-                                                       SZ, P, P, SZ, P]
-        lib.rlk_linear_logp_fwd_save_probs.restype = ctypes.c_int
-        lib.rlk_linear_logp_bwd_saved_probs.argtypes = [P, P, P, P, P, P, SZ, I64, I64, I64, I64,
-                                                        I64, P, I32, P, P, P, SZ, P]
-        lib.rlk_linear_logp_bwd_saved_probs.restype = ctypes.c_int
-        lib.rlk_selftest_wait_timeout.argtypes = [P, P, P, I64, I64, I64, I64, P, P, P, P, SZ, P]
-        lib.rlk_selftest_wait_timeout.restype = ctypes.c_int
-        lib.rlk_shard_sum_bf16.argtypes = [P, I32, I64, P, P]
-        lib.rlk_shard_sum_bf16.restype = ctypes.c_int
-        lib.rlk_quantize_rows_e4m3.argtypes = [P, I64, I64, P, P, P, P]
-        lib.rlk_quantize_rows_e4m3.restype = ctypes.c_int
-        lib.rlk_linear_logp_fwd_fp8.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, P, P, P, P,
-                                                P, SZ, P]
-        lib.rlk_linear_logp_fwd_fp8.restype = ctypes.c_int
-        lib.rlk_linear_logp_bwd_fp8.argtypes = [P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64,
-                                                P, I32, P, P, P, SZ, P]
-        lib.rlk_linear_logp_bwd_fp8.restype = ctypes.c_int
-        lib.rlk_status_string.argtypes = [ctypes.c_int]
-        lib.rlk_status_string.restype = ctypes.c_char_p
-        lib.rlk_version.argtypes = []
-        lib.rlk_version.restype = ctypes.c_char_p
-        _lib = lib
-        return lib
+    lib.rlk_linear_logp_fwd_fp8.restype = ctypes.c_int
+    lib.rlk_linear_logp_bwd_fp8.argtypes = [P, P, P, P, P, P, P, P, P, I64, I64, I64, I64, I64,
+                                            P, I32, P, P, P, SZ, P]
+    lib.rlk_linear_logp_bwd_fp8.restype = ctypes.c_int
+    lib.rlk_status_string.argtypes = [ctypes.c_int]
+    lib.rlk_status_string.restype = ctypes.c_char_p
+    lib.rlk_version.argtypes = []
+    lib.rlk_version.restype = ctypes.c_char_p
+    lib.rlk_debug_checks.argtypes = []
+    lib.rlk_debug_checks.restype = ctypes.c_int32
+    lib.rlk_selftest_bounds_check.argtypes = [P, P, P, I64, I64, I64, I64, P, P, P, P, SZ, P]
+    lib.rlk_selftest_bounds_check.restype = ctypes.c_int
+    return lib
+
+
+@contextlib.contextmanager
+def library(path: str):
+    """Route every call of this module to the librlk.so at `path` (e.g. the debug-checks
+    build) inside the `with` block; the library loaded before is restored afterwards."""
+    global _lib
+    other = _declare(ctypes.CDLL(path))
+    with _lock:
+        prev = _lib
+        _lib = other
+    try:
+        yield other
+    finally:
+        with _lock:
+            _lib = prev
 
 
 def lib():
@@ -440,6 +466,30 @@ def linear_logp_bwd_saved_probs(h: torch.Tensor, W: torch.Tensor, y: torch.Tenso
         _ptr(err_flag), _ptr(ws), nbytes, _stream_handle(stream))
     _check("rlk_linear_logp_bwd_saved_probs", st)
     return dH, dW
+
+
+def debug_checks() -> bool:
+    """True when the loaded library was built with device-side index checks."""
+    return bool(_load().rlk_debug_checks())
+
+
+def selftest_bounds_check(h: torch.Tensor, W: torch.Tensor, y: torch.Tensor, V_true: int,
+                          err_flag: torch.Tensor, stream=None) -> None:
+    """rlk_selftest_bounds_check (debug-checks builds): a forward told that its statistics
+    workspace is one entry short; afterwards err_flag holds RLK_FLAG_BOUNDS."""
+    _need(h, "h", torch.bfloat16, 2)
+    _need(W, "W", torch.bfloat16, 2)
+    _need(y, "y", torch.int64, 1)
+    _need(err_flag, "err_flag", torch.int32, 1)
+    T, H = h.shape
+    V = W.shape[0]
+    ws = _workspace(fwd_workspace_bytes(T, H, V), h.device, None)
+    logp = torch.empty(T, dtype=torch.float32, device=h.device)
+    lse = torch.empty(T, dtype=torch.float32, device=h.device)
+    st = _load().rlk_selftest_bounds_check(_ptr(h), _ptr(W), _ptr(y), T, H, V, int(V_true),
+                                           _ptr(logp), _ptr(lse), _ptr(err_flag), _ptr(ws),
+                                           ws.numel(), _stream_handle(stream))
+    _check("rlk_selftest_bounds_check", st)
 
 
 def selftest_wait_timeout(h: torch.Tensor, W: torch.Tensor, y: torch.Tensor, V_true: int,

@@ -5,7 +5,10 @@ objects are linked into ``_build/librlk.so`` with the CUDA runtime linked
 statically. No torch extension machinery is involved: the library is a plain
 C ABI (include/rlk.h) loaded through ctypes.
 
-``python -m deterministic_token_logprob_gb300.build [--force] [--verbose-ptxas]``
+``python -m deterministic_token_logprob_gb300.build [--force] [--verbose-ptxas] [--debug-checks]``
+
+``--debug-checks`` builds the variant with device-side index and tensor-copy coordinate
+checks (RLK_DEBUG_CHECKS=1, include/rlk.h) into ``_build_debug/librlk.so``.
 """
 from __future__ import annotations
 
@@ -23,6 +26,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "librlk.so")
+OUT_DEBUG = os.path.join(PKG, "_build_debug")
+DEBUG_LIB = os.path.join(OUT_DEBUG, "librlk.so")
 
 SOURCES = ["rlk_api.cu", "rlk_gemm_fwd.cu", "rlk_gemm_dz.cu", "rlk_gemm_dh.cu", "rlk_gemm_dw.cu", "rlk_gemm_fp8.cu",
            "rlk_quant.cu", "rlk_noalloc.cu"]
@@ -56,20 +61,25 @@ def _stamp(extra) -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose_ptxas: bool = False, quiet: bool = True) -> str:
-    """Compile (if sources changed) and return the path of librlk.so."""
-    os.makedirs(OUT, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, quiet: bool = True,
+          debug_checks: bool = False) -> str:
+    """Compile (if sources changed) and return the path of librlk.so (of the debug-checks
+    variant with debug_checks=True)."""
+    out, lib = (OUT_DEBUG, DEBUG_LIB) if debug_checks else (OUT, LIB)
+    os.makedirs(out, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    if debug_checks:
+        extra = extra + ["-DRLK_DEBUG_CHECKS=1"]
     stamp = _stamp(extra)
-    stamp_file = os.path.join(OUT, "librlk.stamp")
-    if not force and os.path.exists(LIB) and os.path.exists(stamp_file):
+    stamp_file = os.path.join(out, "librlk.stamp")
+    if not force and os.path.exists(lib) and os.path.exists(stamp_file):
         with open(stamp_file) as f:
             if f.read().strip() == stamp:
-                return LIB
+                return lib
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(OUT, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(out, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -82,20 +92,22 @@ def build(force: bool = False, verbose_ptxas: bool = False, quiet: bool = True) 
         for obj, log in results:
             if log.strip():
                 print(f"--- {os.path.basename(obj)}\n{log}", file=sys.stderr)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp_file, "w") as f:
         f.write(stamp)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose-ptxas", action="store_true")
+    ap.add_argument("--debug-checks", action="store_true")
     args = ap.parse_args()
-    print(build(force=args.force, verbose_ptxas=args.verbose_ptxas, quiet=False))
+    print(build(force=args.force, verbose_ptxas=args.verbose_ptxas, quiet=False,
+                debug_checks=args.debug_checks))

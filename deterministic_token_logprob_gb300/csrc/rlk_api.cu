@@ -69,6 +69,7 @@ constexpr int kMaxTreeDepth = 16;  // log2(max slots = 8 * 2048) + 1
 
 struct TreeArgs {
   const float* ws;     // [T][n_leaves_local][3]: (m, s, zt) of each (token, leaf)
+  int64_t ws_elems;    // its extent in floats (index checks of debug-checks builds)
   int32_t T;
   int32_t n_leaves_local, leaf0, n_leaves_global;
   int32_t L_ss, P;                // leaves per super-shard, slots per super-shard
@@ -87,8 +88,11 @@ __device__ __forceinline__ Triple load_slot(const TreeArgs& a, int t, int q) {
   const int leaf = ss * a.L_ss + jj;
   const int ll = leaf - a.leaf0;
   if (jj < a.L_ss && leaf < a.n_leaves_global && ll >= 0 && ll < a.n_leaves_local) {
-    const float* p = a.ws + (static_cast<size_t>(t) * a.n_leaves_local + ll) * 3;
-    return Triple{p[0], p[1], p[2]};
+    const size_t i = (static_cast<size_t>(t) * a.n_leaves_local + ll) * 3;
+    if (dbg_ok(i + 3 <= static_cast<size_t>(a.ws_elems), a.err_flag)) {
+      const float* p = a.ws + i;
+      return Triple{p[0], p[1], p[2]};
+    }
   }
   return identity_triple();
 }
@@ -212,7 +216,7 @@ __global__ void __launch_bounds__(DZS_THREADS)
     dz_from_logits_kernel(const float* __restrict__ z, int64_t z_ld, const int64_t* __restrict__ y,
                           const float* __restrict__ lse, const float* __restrict__ g, int Vd,
                           int V_valid, int vocab_start, int V_true, uint16_t* __restrict__ dz,
-                          int64_t dz_ld, int32_t* err_flag) {
+                          int64_t dz_ld, int32_t* err_flag, int64_t z_elems, int64_t dz_elems) {
   const int t = blockIdx.x;
   const int64_t yt = y[t];
   const bool yvalid = yt >= 0 && yt < V_true;
@@ -229,10 +233,13 @@ __global__ void __launch_bounds__(DZS_THREADS)
 #pragma unroll
     for (int u = 0; u < DZS_UNROLL; ++u) {
       const int c0 = base + u * DZS_THREADS * 8;
-      if (c0 < n_valid) {
+      if (c0 < n_valid &&
+          dbg_ok(static_cast<size_t>(t) * z_ld + c0 + 8 <= static_cast<size_t>(z_elems), err_flag)) {
         const float4* zp = reinterpret_cast<const float4*>(zr + c0);
         zv[u][0] = zp[0];
         zv[u][1] = zp[1];
+      } else {
+        zv[u][0] = zv[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
 #pragma unroll
@@ -255,7 +262,8 @@ __global__ void __launch_bounds__(DZS_THREADS)
       w.y = pack_bf16x2(d[2], d[3]);
       w.z = pack_bf16x2(d[4], d[5]);
       w.w = pack_bf16x2(d[6], d[7]);
-      *reinterpret_cast<uint4*>(dr + c0) = w;
+      if (dbg_ok(static_cast<size_t>(t) * dz_ld + c0 + 8 <= static_cast<size_t>(dz_elems), err_flag))
+        *reinterpret_cast<uint4*>(dr + c0) = w;
     }
   }
 }
@@ -266,7 +274,8 @@ __global__ void __launch_bounds__(DZS_THREADS)
     dz_from_probs_kernel(const uint16_t* __restrict__ pb, const float* __restrict__ pm, int64_t ld,
                          const int64_t* __restrict__ y, const float* __restrict__ lse,
                          const float* __restrict__ g, int Vd, int V_valid, int vocab_start,
-                         int V_true, uint16_t* __restrict__ dz, int64_t dz_ld, int32_t* err_flag) {
+                         int V_true, uint16_t* __restrict__ dz, int64_t dz_ld, int32_t* err_flag,
+                         int64_t p_elems, int64_t pm_elems, int64_t dz_elems) {
   const int t = blockIdx.x;
   const int64_t yt = y[t];
   const bool yvalid = yt >= 0 && yt < V_true;
@@ -284,9 +293,15 @@ __global__ void __launch_bounds__(DZS_THREADS)
 #pragma unroll
     for (int u = 0; u < DZS_UNROLL; ++u) {
       const int c0 = base + u * DZS_THREADS * 8;
-      if (c0 < n_valid) {
+      if (c0 < n_valid &&
+          dbg_ok(static_cast<size_t>(t) * ld + c0 + 8 <= static_cast<size_t>(p_elems) &&
+                     static_cast<size_t>(t) * (ld / 64) + c0 / 64 < static_cast<size_t>(pm_elems),
+                 err_flag)) {
         raw[u] = *reinterpret_cast<const uint4*>(pr + c0);
         mx[u] = pmr[c0 / 64];
+      } else {
+        raw[u] = make_uint4(0u, 0u, 0u, 0u);
+        mx[u] = 0.f;
       }
     }
 #pragma unroll
@@ -312,7 +327,8 @@ __global__ void __launch_bounds__(DZS_THREADS)
       o.y = pack_bf16x2(d[2], d[3]);
       o.z = pack_bf16x2(d[4], d[5]);
       o.w = pack_bf16x2(d[6], d[7]);
-      *reinterpret_cast<uint4*>(dr + c0) = o;
+      if (dbg_ok(static_cast<size_t>(t) * dz_ld + c0 + 8 <= static_cast<size_t>(dz_elems), err_flag))
+        *reinterpret_cast<uint4*>(dr + c0) = o;
     }
   }
 }
@@ -525,7 +541,7 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
                     rlk_lse_partial* partial, float* z_saved, size_t z_saved_bytes,
                     int32_t* err_flag, void* workspace, size_t workspace_bytes, void* stream,
                     int32_t stall_stage = -1, void* p_saved = nullptr, size_t p_saved_bytes = 0,
-                    const Fp8In* f8 = nullptr) {
+                    const Fp8In* f8 = nullptr, int64_t ws_entries_short = 0) {
   rlk_status st = common_checks(h, W, y, T, H, V_local, vocab_start, V_true);
   if (st != RLK_OK) return st;
   if (f8 && (H % 16 != 0 || !f8->W_scale || !aligned16(f8->W_scale) || (T > 0 && !f8->h_scale)))
@@ -549,6 +565,8 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* ws = static_cast<float*>(workspace);  // [T][n_leaves_local][3] (fits in 3 * arr)
+  // its extent for the index checks (the bounds self-test understates it by whole entries)
+  const int64_t ws_elems = (T * g.n_leaves_local - ws_entries_short) * 3;
 
   if (g.n_leaves_local > 0) {
     const int eb = f8 ? 1 : 2;  // element bytes of h / W
@@ -573,12 +591,14 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
     }
     a.y = y;
     a.ws = ws;
+    a.ws_elems = ws_elems;
     a.z_out = z_saved;
     a.z_ld = round_up(V_local, BN);
     if (z_saved && !encode_out(&maps, z_saved, a.z_ld, T, 4)) return RLK_ERR_CUDA;
     if (p_saved) {
       a.p_out = static_cast<uint16_t*>(p_saved);
       a.pm_out = reinterpret_cast<float*>(static_cast<char*>(p_saved) + saved_probs_offset(T, V_local));
+      a.pm_elems = T * (a.z_ld / 64);
       if (!encode_out(&maps, p_saved, a.z_ld, T, 2)) return RLK_ERR_CUDA;
     }
     a.err_flag = err_flag;
@@ -589,6 +609,7 @@ rlk_status fwd_impl(const void* h, const void* W, const int64_t* y, int64_t T, i
 
   TreeArgs ta;
   ta.ws = ws;
+  ta.ws_elems = ws_elems;
   ta.T = static_cast<int32_t>(T);
   ta.n_leaves_local = static_cast<int32_t>(g.n_leaves_local);
   ta.leaf0 = static_cast<int32_t>(g.leaf0);
@@ -646,6 +667,18 @@ rlk_status rlk_linear_logp_fwd_save_probs(const void* h, const void* W, const in
   if (T > 0 && !p_saved) return RLK_ERR_INVALID_ARG;
   return fwd_impl(h, W, y, T, H, V_local, vocab_start, V_true, logp, lse, partial, nullptr, 0,
                   err_flag, workspace, workspace_bytes, stream, -1, p_saved, p_saved_bytes);
+}
+
+int32_t rlk_debug_checks(void) { return kDebugChecks ? 1 : 0; }
+
+rlk_status rlk_selftest_bounds_check(const void* h, const void* W, const int64_t* y, int64_t T,
+                                     int64_t H, int64_t V, int64_t V_true, float* logp, float* lse,
+                                     int32_t* err_flag, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  if (!kDebugChecks) return RLK_ERR_UNSUPPORTED;
+  if (!err_flag || T <= 0) return RLK_ERR_INVALID_ARG;
+  return fwd_impl(h, W, y, T, H, V, 0, V_true, logp, lse, nullptr, nullptr, 0, err_flag, workspace,
+                  workspace_bytes, stream, -1, nullptr, 0, nullptr, /*ws_entries_short=*/1);
 }
 
 rlk_status rlk_selftest_wait_timeout(const void* h, const void* W, const int64_t* y, int64_t T,
@@ -735,13 +768,14 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
         static_cast<const uint16_t*>(p_saved),
         reinterpret_cast<const float*>(static_cast<const char*>(p_saved) + saved_probs_offset(T, V_local)),
         Vd, y, lse, g, static_cast<int>(Vd), static_cast<int>(V_valid),
-        static_cast<int>(vocab_start), static_cast<int>(V_true), dz, Vd, err_flag);
+        static_cast<int>(vocab_start), static_cast<int>(V_true), dz, Vd, err_flag, T * Vd,
+        T * (Vd / 64), T * Vd);
     if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
   } else if (z_saved) {
     const int64_t V_valid = std::max<int64_t>(0, std::min<int64_t>(V_true - vocab_start, V_local));
     dz_from_logits_kernel<<<static_cast<unsigned>(T), DZS_THREADS, 0, s>>>(  // one block per row
         z_saved, Vd, y, lse, g, static_cast<int>(Vd), static_cast<int>(V_valid),
-        static_cast<int>(vocab_start), static_cast<int>(V_true), dz, Vd, err_flag);
+        static_cast<int>(vocab_start), static_cast<int>(V_true), dz, Vd, err_flag, T * Vd, T * Vd);
     if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
   } else {
     const int eb = f8 ? 1 : 2;  // element bytes of the logit operands
@@ -799,6 +833,8 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
       a.out_f32 = dH_fp32_partial ? 1 : 0;
       if (!dH_fp32_partial && a.n_kb > KC_BLOCKS)
         a.acc_scratch = reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_dz_bytes(T, V_local));
+      a.out_elems = T * H;
+      a.run_elems = (dH_fp32_partial || a.acc_scratch) ? T * H : 0;
       // TMA stores of the final values, unless the fp32 output is itself the running sum
       // of several K chunks (then every chunk updates it with plain loads and stores)
       if (!dH_fp32_partial || a.n_kb <= KC_BLOCKS) {
@@ -830,6 +866,7 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
     a.out_rows = static_cast<int32_t>(V_local);
     a.out_cols = static_cast<int32_t>(H);
     a.out_f32 = 1;
+    a.out_elems = a.run_elems = V_local * H;
     if (a.n_kb <= KC_BLOCKS) {  // one K chunk: TMA stores (several: dW is the running sum)
       if (!encode_out(&maps, dW, H, V_local, 4)) return RLK_ERR_CUDA;
       a.out_tma = 1;

@@ -245,7 +245,10 @@ __device__ __forceinline__ int a_boxes(int rows_left) {
 // fetched by one copy of the 3-D view when `wide`, else by two 2-D copies. mn is a
 // multiple of 128.
 __device__ __forceinline__ void load_mn_tile(uint8_t* dst, const CUtensorMap* m, int32_t wide,
-                                             uint32_t bar, int mn, int k0, uint64_t pol) {
+                                             uint32_t bar, int mn, int k0, uint64_t pol,
+                                             int32_t* err_flag) {
+  // the innermost coordinate of a tensor copy must be a multiple of 16 bytes (8 bf16)
+  if (!dbg_ok((mn & 7) == 0, err_flag)) mn &= ~7;
   if (wide) {
     tma_load_3d_pair(dst, m, bar, 0, k0, mn / 64, pol);
   } else {
@@ -303,7 +306,10 @@ __device__ void producer_loop(const TileMaps& maps, const GemmArgs& a, uint8_t* 
           ++issued;  // self-test: this stage's bytes never arrive
           continue;
         }
-        const int k0 = kb * Operands<MODE>::K_PER_STAGE;
+        int k0 = kb * Operands<MODE>::K_PER_STAGE;
+        // K-major copies start at k0 along their innermost axis: 16-byte aligned (E4M3 codes
+        // are 1 byte, bf16 2); a failed check copies from the aligned coordinate below
+        if (!dbg_ok(((k0 * (is_e4m3<MODE> ? 1 : 2)) & 15) == 0, a.err_flag)) k0 &= ~15;
         if constexpr (kAPerRow) {
           if (boxes_mine == BM / A_BOX_ROWS) {            // h / dz, K-major box 64 x 128
             tma_load_2d_pair(sA, &maps.a_full, bar, k0, am, polA);
@@ -312,12 +318,12 @@ __device__ void producer_loop(const TileMaps& maps, const GemmArgs& a, uint8_t* 
               tma_load_2d_pair(sA + q * A_BOX_BYTES, &maps.a, bar, k0, am + q * A_BOX_ROWS, polA);
           }
         } else {                                          // dz[k0.., am..], MN-major 128 x 64
-          load_mn_tile(sA, &maps.a, a.a_mn_wide, bar, am, k0, polA);
+          load_mn_tile(sA, &maps.a, a.a_mn_wide, bar, am, k0, polA, a.err_flag);
         }
         if constexpr (kZ) {
           tma_load_2d_pair(sB, &maps.b, bar, k0, bn, polB);   // W, K-major box 128 rows x 128 B
         } else {                                          // W (dH) / h (dW)[k0.., bn..], MN-major
-          load_mn_tile(sB, &maps.b, a.b_mn_wide, bar, bn, k0, polB);
+          load_mn_tile(sB, &maps.b, a.b_mn_wide, bar, bn, k0, polB, a.err_flag);
         }
         ++issued;
       }
@@ -550,10 +556,12 @@ __device__ __forceinline__ void stage_chunk(uint32_t buf, int lane, int j, uint4
 // Every lane of the warp calls it after staging its row; (x, y) = the box's first column
 // and row in the output.
 __device__ __forceinline__ void stage_store(BoxStager& S, uint32_t buf, int lane, const CUtensorMap* m,
-                                            int x, int y, uint64_t pol) {
+                                            int x, int y, uint64_t pol, int32_t* err_flag) {
   fence_proxy_async_smem();
   __syncwarp();
-  if (lane == 0) {
+  // a store starts at a non-negative, 16-byte aligned innermost coordinate (x is in
+  // elements of 2 or 4 bytes: a multiple of 8 is aligned for both)
+  if (lane == 0 && dbg_ok(x >= 0 && y >= 0 && (x & 7) == 0, err_flag)) {
     tma_store_2d(m, buf, x, y, pol);
     bulk_commit_group();
   }
@@ -637,7 +645,7 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
               const uint32_t buf = stage_begin(stg, lane);
 #pragma unroll
               for (int q = 0; q < 8; ++q) stage_chunk(buf, lane, q, f32x4_bits(v + 32 * b + 4 * q));
-              stage_store(stg, buf, lane, out_map, lc + ch + 32 * b, m0 + row0_off, pol_out);
+              stage_store(stg, buf, lane, out_map, lc + ch + 32 * b, m0 + row0_off, pol_out, a.err_flag);
             }
           }
           if constexpr (keep_p) {  // saved probabilities: bf16 e(z - m) and the fp32 running max m
@@ -645,8 +653,11 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
             const uint32_t buf = stage_begin(stg, lane);
 #pragma unroll
             for (int q = 0; q < 8; ++q) stage_chunk(buf, lane, q, pack8_bf16(v + 8 * q));
-            stage_store(stg, buf, lane, out_map, lc + ch, m0 + row0_off, pol_out);
-            if (t < a.T) a.pm_out[static_cast<size_t>(t) * (a.z_ld / 64) + (lc + ch) / 64] = st.m;
+            stage_store(stg, buf, lane, out_map, lc + ch, m0 + row0_off, pol_out, a.err_flag);
+            if (t < a.T) {
+              const size_t i = static_cast<size_t>(t) * (a.z_ld / 64) + (lc + ch) / 64;
+              if (dbg_ok(i < static_cast<size_t>(a.pm_elems), a.err_flag)) a.pm_out[i] = st.m;
+            }
           } else {
             fwd_chunk(v, vcols - ch, tl - ch, st);
           }
@@ -688,7 +699,7 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
             const uint32_t buf = stage_begin(stg, lane);
 #pragma unroll
             for (int q = 0; q < 8; ++q) stage_chunk(buf, lane, q, pack8_bf16(v + 8 * q));
-            stage_store(stg, buf, lane, out_map, nt0 + ch, m0 + row0_off, pol_out);
+            stage_store(stg, buf, lane, out_map, nt0 + ch, m0 + row0_off, pol_out, a.err_flag);
           }
         }
       } else {
@@ -705,11 +716,13 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
           tmem_ld64(taddr + ch, v);
           const int col = n0 + ch;
           if (row_ok && col < a.out_cols && nchunks > 1) {
-            float* p = run + static_cast<size_t>(t) * a.out_ld + col;
+            const size_t off = static_cast<size_t>(t) * a.out_ld + col;
+            float* p = run + off;
             if (!first) {
 #pragma unroll
               for (int q = 0; q < 16; ++q)
-                if (col + 4 * q < a.out_cols) {
+                if (col + 4 * q < a.out_cols &&
+                    dbg_ok(off + 4 * q + 4 <= static_cast<size_t>(a.run_elems), a.err_flag)) {
                   const float4 r = *reinterpret_cast<const float4*>(p + 4 * q);
                   v[4 * q] = __fadd_rn(r.x, v[4 * q]);
                   v[4 * q + 1] = __fadd_rn(r.y, v[4 * q + 1]);
@@ -720,7 +733,8 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
             if (!last) {
 #pragma unroll
               for (int q = 0; q < 16; ++q)
-                if (col + 4 * q < a.out_cols)
+                if (col + 4 * q < a.out_cols &&
+                    dbg_ok(off + 4 * q + 4 <= static_cast<size_t>(a.run_elems), a.err_flag))
                   *reinterpret_cast<float4*>(p + 4 * q) =
                       make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
               continue;
@@ -738,30 +752,34 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
                   const uint32_t buf = stage_begin(stg, lane);
 #pragma unroll
                   for (int q = 0; q < 8; ++q) stage_chunk(buf, lane, q, f32x4_bits(v + 32 * b + 4 * q));
-                  stage_store(stg, buf, lane, out_map, col + 32 * b, m0 + row0_off, pol_out);
+                  stage_store(stg, buf, lane, out_map, col + 32 * b, m0 + row0_off, pol_out, a.err_flag);
                 }
               } else {
                 const uint32_t buf = stage_begin(stg, lane);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) stage_chunk(buf, lane, q, pack8_bf16(v + 8 * q));
-                stage_store(stg, buf, lane, out_map, col, m0 + row0_off, pol_out);
+                stage_store(stg, buf, lane, out_map, col, m0 + row0_off, pol_out, a.err_flag);
               }
             }
           } else if (!a.out_tma && row_ok && col < a.out_cols) {
+            const size_t off = static_cast<size_t>(t) * a.out_ld + col;
             if (a.out_f32) {
-              float* p = static_cast<float*>(a.out) + static_cast<size_t>(t) * a.out_ld + col;
+              float* p = static_cast<float*>(a.out) + off;
 #pragma unroll
               for (int q = 0; q < 16; ++q)
-                if (col + 4 * q < a.out_cols)
+                if (col + 4 * q < a.out_cols &&
+                    dbg_ok(off + 4 * q + 4 <= static_cast<size_t>(a.out_elems), a.err_flag))
                   st_global_v4_hint(p + 4 * q,
                                     make_uint4(__float_as_uint(v[4 * q]), __float_as_uint(v[4 * q + 1]),
                                                __float_as_uint(v[4 * q + 2]), __float_as_uint(v[4 * q + 3])),
                                     pol_out);
             } else {
-              uint16_t* p = static_cast<uint16_t*>(a.out) + static_cast<size_t>(t) * a.out_ld + col;
+              uint16_t* p = static_cast<uint16_t*>(a.out) + off;
 #pragma unroll
               for (int q = 0; q < 8; ++q)
-                if (col + 8 * q < a.out_cols) st_global_v4_hint(p + 8 * q, pack8_bf16(v + 8 * q), pol_out);
+                if (col + 8 * q < a.out_cols &&
+                    dbg_ok(off + 8 * q + 8 <= static_cast<size_t>(a.out_elems), a.err_flag))
+                  st_global_v4_hint(p + 8 * q, pack8_bf16(v + 8 * q), pol_out);
             }
           }
         }
@@ -777,10 +795,13 @@ __device__ void epilogue_loop(const GemmArgs& a, uint64_t* acc_full, uint64_t* a
       if (ok && t < a.T) {
         int leaf_local, pm;
         item_unit_pm(a, a.n_leaves, item, leaf_local, pm);
-        float* o = a.ws + (static_cast<size_t>(t) * a.n_leaves + leaf_local) * 3;
-        o[0] = st.m;
-        o[1] = st.s;
-        o[2] = st.zt;
+        const size_t i = (static_cast<size_t>(t) * a.n_leaves + leaf_local) * 3;
+        if (dbg_ok(i + 3 <= static_cast<size_t>(a.ws_elems), a.err_flag)) {
+          float* o = a.ws + i;
+          o[0] = st.m;
+          o[1] = st.s;
+          o[2] = st.zt;
+        }
       }
     }
   }

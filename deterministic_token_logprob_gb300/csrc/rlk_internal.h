@@ -6,7 +6,28 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+// Device-side index and tensor-copy coordinate checks (debug-checks builds only; see
+// rlk_debug_checks in rlk.h). Off, every check below compiles to nothing.
+#ifndef RLK_DEBUG_CHECKS
+#define RLK_DEBUG_CHECKS 0
+#endif
+
 namespace rlk {
+
+constexpr bool kDebugChecks = RLK_DEBUG_CHECKS != 0;
+constexpr int32_t kFlagBounds = 8;  // RLK_FLAG_BOUNDS
+
+// True when the access may go ahead. In a debug-checks build a failed check ORs the bounds
+// flag into the caller's flag (if any) and returns false; otherwise it is always true.
+__device__ __forceinline__ bool dbg_ok(bool cond, int32_t* err_flag) {
+  if constexpr (kDebugChecks) {
+    if (!cond) {
+      if (err_flag) atomicOr(err_flag, kFlagBounds);
+      return false;
+    }
+  }
+  return true;
+}
 
 // Tile constants: part of the numerical contract (they fix the K steps and the
 // vocab walk), identical for every shape.
@@ -118,6 +139,10 @@ struct GemmArgs {
   const float* a_scale = nullptr;
   const float* b_scale = nullptr;
   int32_t n_mt = 0, n_nt = 0;      // dH / dW: 256-row pair tiles along M, 256-column tiles along N
+  // Extents (in elements) of the buffers the epilogue addresses by index, for the checks of
+  // debug-checks builds: fwd statistics, saved running maxima, the running sum of several K
+  // chunks (the fp32 output or acc_scratch), the plain-store output.
+  int64_t ws_elems = 0, pm_elems = 0, run_elems = 0, out_elems = 0;
   // Self-test only (rlk_selftest_wait_timeout): the even CTA arms its `stall_stage`-th
   // stage but issues none of its copies, so the wait on that stage cannot complete.
   int32_t stall_stage = -1;

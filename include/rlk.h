@@ -93,6 +93,8 @@ typedef enum {
 #define RLK_FLAG_BAD_TARGET 1
 #define RLK_FLAG_TIMEOUT 2
 #define RLK_FLAG_NONFINITE 4 /* rlk_quantize_rows_e4m3: a row held a NaN or an infinity */
+#define RLK_FLAG_BOUNDS 8    /* debug-checks builds only: an index or tensor-copy coordinate
+                                check failed; the access was skipped (see rlk_debug_checks) */
 
 /* tiling constants that are part of the numerical contract */
 #define RLK_LEAF_WIDTH 1024
@@ -400,6 +402,32 @@ RLK_API rlk_status rlk_linear_logp_fwd_noalloc(const void* h, const void* W, con
  * trap or hang is involved, and the CUDA context stays usable afterwards.
  */
 RLK_API rlk_status rlk_selftest_wait_timeout(const void* h, const void* W, const int64_t* y,
+                                             int64_t T, int64_t H, int64_t V, int64_t V_true,
+                                             float* logp, float* lse, int32_t* err_flag,
+                                             void* workspace, size_t workspace_bytes,
+                                             void* stream);
+
+/*
+ * Debug-checks builds. The library can also be compiled with device-side checks
+ * (RLK_DEBUG_CHECKS=1; `python -m deterministic_token_logprob_gb300.build --debug-checks`
+ * writes _build_debug/librlk.so): before every global-memory access whose address the
+ * kernels compute from an index (statistics, saved maxima, running sums, plain output
+ * stores, the dz passes, the leaf-tree reads) they check the index against the extent of
+ * the buffer, and before every tensor copy they check the rules of its coordinates (the
+ * innermost one a multiple of 16 bytes, a store's never negative). A failed check ORs
+ * RLK_FLAG_BOUNDS into *err_flag and skips the access instead of trapping, so the context
+ * stays usable. Results of a build with checks are bit-identical to the plain build's.
+ *
+ * rlk_debug_checks: 1 for a library built with the checks, else 0.
+ * rlk_selftest_bounds_check: the unsharded forward (arguments as rlk_linear_logp_fwd) told
+ * that its statistics workspace is one (token, leaf) entry shorter than it is, so the last
+ * entry's store and read fail their checks: afterwards *err_flag (required) holds
+ * RLK_FLAG_BOUNDS, and every access stayed inside the real buffers. logp / lse are
+ * undefined. Without the checks it returns RLK_ERR_UNSUPPORTED and launches nothing.
+ */
+RLK_API int32_t rlk_debug_checks(void);
+
+RLK_API rlk_status rlk_selftest_bounds_check(const void* h, const void* W, const int64_t* y,
                                              int64_t T, int64_t H, int64_t V, int64_t V_true,
                                              float* logp, float* lse, int32_t* err_flag,
                                              void* workspace, size_t workspace_bytes,

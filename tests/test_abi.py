@@ -243,3 +243,24 @@ def test_fp8_argument_errors(lib):
     assert b8(H=72) == INVALID
     assert b8(Ws=None) == INVALID
     assert b8(nb=bws - 1) == WORKSPACE
+
+
+def test_debug_checks_variant_builds_and_exports_the_same_symbols(lib):
+    # the variant with device-side index checks (compiled here, run by the GPU tests)
+    import subprocess
+    from deterministic_token_logprob_gb300 import _binding, build
+    path = build.build(debug_checks=True)
+    assert path != build.LIB
+
+    def exported(p):
+        out = subprocess.run(["nm", "-D", "--defined-only", p], capture_output=True, text=True).stdout
+        return {ln.split()[-1] for ln in out.splitlines() if " T " in ln and ln.split()[-1].startswith("rlk_")}
+    assert exported(path) == exported(build.LIB) == set(declared_functions())
+    dbg = _binding._declare(ctypes.CDLL(path))
+    assert dbg.rlk_debug_checks() == 1
+    assert lib.rlk_debug_checks() == 0
+    # without the checks the bounds self-test is refused before anything touches CUDA
+    args = (FAKE, FAKE, FAKE, 4, 64, 4096, 4096, FAKE, FAKE, FAKE, FAKE, 1 << 30, None)
+    assert lib.rlk_selftest_bounds_check(*args) == UNSUPPORTED
+    assert dbg.rlk_selftest_bounds_check(FAKE, FAKE, FAKE, 4, 64, 4096, 4096, FAKE, FAKE, None, FAKE,
+                                         1 << 30, None) == INVALID   # err_flag is required
