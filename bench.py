@@ -3,16 +3,26 @@ Qwen3-8B output-layer shape, with the tensor-core roofline fraction.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl rlk|reference]
                 [--workload qwen3_8b|qwen3_30b_tp2|tiny] [--quick]
+python bench.py --case fwd|dz|dh|dw|fwd8|dz8 [--tokens T] [--vocab V]
+python bench.py --record-traffic NCU_CSV --traffic-command CMD
 
 A step is one pass of the whole path over one synthetic batch: the fused
 forward (tile GEMM + online statistics + fixed-tree merge; for the sharded
 workload one call per vocab shard plus rlk_lse_merge) and the backward (dz
-recompute, dH, dW; sharded: per shard plus the fixed-order dH sum). N > 1
-runs one independent batch per rank (weak scaling; no collective on the data
-path, only a barrier and a max of the elapsed times). Rank 0 prints one JSON line.
+recompute, dH, dW; sharded: per shard plus the fixed-order dH sum), the
+backward launched as its three stages so that a CUDA event between the calls
+times each GEMM inside the step. N > 1 runs one independent batch per rank
+(weak scaling; no collective on the data path, only a barrier and a max of
+the elapsed times). Rank 0 prints one JSON line; at N = 1 it also carries the
+small-batch and tiny legs (run first), the end-to-end leg from host buffers,
+the forward-only, saved-logits, saved-probabilities and FP8 legs, the two-shard
+Qwen3-30B step, one rank's calls of that split, and the CPU oracle baseline.
 
 --impl reference times the fp64 CPU oracle on the host cores instead (each
 step a bounded sample of the same workload, extrapolated per token).
+--case times one stage alone (per-kernel timings, small ncu captures).
+--record-traffic writes the per-launch DRAM bytes of an ncu capture of the
+step to profiles/traffic_qwen3_8b.json together with the library sources' hash.
 """
 from __future__ import annotations
 
