@@ -482,10 +482,12 @@ def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int)
     }
     line.update(first_legs)
 
-    if rank == 0 and world == 1 and not args.quick:
+    if not args.quick:
         # the end-to-end step first, right after the device-timed loop, so that both run in
-        # the same thermal and power state; the other legs follow
-        line["e2e"] = e2e(rlk, torch, path, wr, d, device, args, gpu_uuid(torch, device))
+        # the same thermal and power state (every rank: its own batch); the other legs follow
+        line["e2e"] = e2e(rlk, torch, path, wr, d, device, args,
+                          gpu_uuid(torch, device) if rank == 0 else None, world)
+    if rank == 0 and world == 1 and not args.quick:
         if w.name == "qwen3_8b":  # legs defined on the Qwen3-8B weight
             line["fwd_only"] = fwd_only(rlk, torch, W_bits, path, device, args, peak)
             line["saved_logits"] = saved_logits_leg(rlk, torch, path, wr, device, args, peak, peak_sus)
@@ -932,13 +934,15 @@ def fwd_only(rlk, torch, W_bits, path, device, args, peak):
             "frac_of_burst": tf / peak, "steps": K}
 
 
-def e2e(rlk, torch, path, w, d, device, args, gpu_id=None):
+def e2e(rlk, torch, path, w, d, device, args, gpu_id=None, world=1):
     """Same step through the public API from pinned host buffers: every step copies
     its inputs (h, y, g) host -> device, runs the C-ABI calls and copies its result
     (logp) device -> host, all inside the timed region. The weight W is model state
     and stays resident, as in a training step. Like a training input pipeline, the
     copies of step k+1's inputs run on a second stream into a second set of device
-    buffers while step k computes (double buffering, ordered by events)."""
+    buffers while step k computes (double buffering, ordered by events). With several
+    ranks, each runs its own batch between two barriers, and the job's throughput is
+    every rank's tokens over the slowest rank's time."""
     h_host = torch.from_numpy(d["h"].view(np.int16)).view(torch.bfloat16).pin_memory()
     y_host = torch.from_numpy(d["y"]).pin_memory()
     g_host = torch.from_numpy(d["g"]).pin_memory()
@@ -981,6 +985,10 @@ def e2e(rlk, torch, path, w, d, device, args, gpu_id=None):
     sampler = ClockSampler(gpu_id) if gpu_id else None
     if sampler:
         sampler.wait_running()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    if sampler:
         sampler.mark_start()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(compute)
@@ -989,15 +997,21 @@ def e2e(rlk, torch, path, w, d, device, args, gpu_id=None):
     torch.cuda.synchronize(device)
     if sampler:
         sampler.mark_end()
+    if world > 1:
+        torch.distributed.barrier()
     clocks = sampler.stop() if sampler else None
     path.h, path.y, path.g = sets[0]
-    ms = a.elapsed_time(b) / K
-    return {"value": w.T / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms,
-            "pipeline": "inputs of step k+1 copied on a second stream while step k computes",
-            "d2h": ("logp only; dH and dW stay on the device, where the model's backward and the "
-                    "optimizer consume them"),
-            "clocks": clocks}
+    ms = max_over_ranks(a.elapsed_time(b), world, device) / K
+    out = {"value": w.T * world / (ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d * world, "d2h_bytes_per_step": d2h * world, "ms_per_step": ms,
+           "pipeline": "inputs of step k+1 copied on a second stream while step k computes",
+           "d2h": ("logp only; dH and dW stay on the device, where the model's backward and the "
+                   "optimizer consume them"),
+           "clocks": clocks}
+    if world > 1:
+        out["h2d_bytes_per_step_per_rank"] = h2d
+        out["d2h_bytes_per_step_per_rank"] = d2h
+    return out
 
 
 def run_case(args):
