@@ -62,3 +62,67 @@ def test_committed_traffic_record_is_well_formed():
     for stage, k in rec["kernels"].items():
         assert stage in ("fwd", "dz", "dH", "dW") and k["launches"] >= 1
         assert k["traffic_bytes_per_launch"] > 0
+
+
+class _FakeRlk:
+    """Records the binding calls bench.Path makes (no GPU, no library)."""
+    RLK_BWD_DZ, RLK_BWD_DH, RLK_BWD_DW = 1, 2, 4
+
+    def __init__(self):
+        self.calls = []
+
+    def fwd_workspace_bytes(self, T, H, n):
+        return 16
+
+    bwd_workspace_bytes = fwd_workspace_bytes
+
+    def linear_logp_fwd(self, h, W, y, V_true, vocab_start=0, partial=False, **kw):
+        self.calls.append(("fwd", vocab_start, W.shape[0], partial))
+
+    def linear_logp_bwd(self, h, W, y, lse, g, V_true, vocab_start=0, dH_fp32_partial=False,
+                        stages=None, **kw):
+        self.calls.append(("bwd", vocab_start, W.shape[0], dH_fp32_partial, stages))
+
+    def lse_merge(self, parts, **kw):
+        self.calls.append(("merge", parts.shape[0]))
+
+    def shard_sum_bf16(self, parts, **kw):
+        self.calls.append(("sum", parts.shape[0]))
+
+
+def _path(w):
+    import numpy as np
+    import torch
+    d = {"h": np.zeros((w.T, w.H), np.uint16), "W": np.zeros((w.V, w.H), np.uint16),
+         "y": np.zeros(w.T, np.int64), "g": np.zeros(w.T, np.float32)}
+    fake = _FakeRlk()
+    return bench.Path(fake, torch, w, d, torch.device("cpu")), fake
+
+
+def test_staged_step_calls_every_stage_once_in_order():
+    import workloads
+    w = workloads.Workload("s", T=8, H=16, V=64, V_true=60)
+    path, fake = _path(w)
+    calls = path.staged_calls()
+    assert [n for n, _ in calls] == ["fwd", "dz", "dH", "dW"]
+    for _, fn in calls:
+        fn()
+    assert fake.calls == [("fwd", 0, 64, False), ("bwd", 0, 64, False, 1), ("bwd", 0, 64, False, 2),
+                          ("bwd", 0, 64, False, 4)]
+    assert path.launches_per_step() == 5
+
+
+def test_staged_sharded_step_attributes_each_shard_launch_to_its_stage():
+    import workloads
+    w = workloads.Workload("s2", T=8, H=16, V=20480, V_true=20000, shards=((0, 12288), (12288, 8192)))
+    path, fake = _path(w)
+    calls = path.staged_calls()
+    assert [n for n, _ in calls] == ["fwd", "fwd", "merge", "dz", "dH", "dW", "dz", "dH", "dW", "sum"]
+    for _, fn in calls:
+        fn()
+    assert fake.calls == [("fwd", 0, 12288, True), ("fwd", 12288, 8192, True), ("merge", 2),
+                          ("bwd", 0, 12288, True, 1), ("bwd", 0, 12288, True, 2),
+                          ("bwd", 0, 12288, True, 4), ("bwd", 12288, 8192, True, 1),
+                          ("bwd", 12288, 8192, True, 2), ("bwd", 12288, 8192, True, 4), ("sum", 2)]
+    # one step launches: per shard 2 forward kernels and 3 backward kernels, the merge, the sum
+    assert path.launches_per_step() == 2 * 2 + 1 + 3 * 2 + 1
