@@ -193,3 +193,42 @@ def test_qwen3_8b_saved_probs_close_to_recompute(rlk, W8b):
     eW = float((dW2 - dW).norm() / dW.norm())
     assert eH <= 1e-2 and eW <= 1e-2, (eH, eW)
     assert torch.all(dW2[w.V_true:] == 0)
+
+
+def test_qwen3_30b_rank_call_sizes_batch_invariant(rlk, oracle_mod):
+    # The token counts per call of the pages' own TP = 2 measurement (796, 1820, 6827) on the
+    # Qwen3-30B-A3B output layer, through the two-shard path (shard statistics + merge; fp32 dH
+    # partials + ordered sum). The smaller batches are prefixes of the largest, so every token
+    # must get the same logp, lse and dH bits in all three calls; the merged results equal the
+    # unsharded call; sampled rows match the oracle.
+    w = workloads.QWEN3_30B_TP2
+    bits = workloads.make_W(w.V, w.H, 0)
+    W = dev_bf16(bits)
+    Tmax = 6827
+    hb = workloads.make_h(Tmax, w.H, 21)
+    yb = workloads.make_y(Tmax, w.V_true, 21)
+    g = np.random.default_rng(22).standard_normal(Tmax).astype(np.float32)
+    seen = {}
+    for T in (796, 1820, Tmax):
+        h, y, gd = dev_bf16(hb[:T]), dev(yb[:T]), dev(g[:T])
+        parts = torch.stack([rlk.linear_logp_fwd(h, W[a:a + n], y, w.V_true, vocab_start=a,
+                                                 partial=True) for a, n in w.shards])
+        logp, lse = rlk.lse_merge(parts)
+        ulogp, ulse = rlk.linear_logp_fwd(h, W, y, w.V_true)
+        assert torch.equal(logp, ulogp) and torch.equal(lse, ulse), T
+        dHp = torch.stack([rlk.linear_logp_bwd(h, W[a:a + n], y, lse, gd, w.V_true, vocab_start=a,
+                                               dH_fp32_partial=True, want_dW=False)[0]
+                           for a, n in w.shards])
+        dH = rlk.shard_sum_bf16(dHp)
+        seen[T] = (logp.cpu().numpy(), lse.cpu().numpy(), dH.view(torch.int16).cpu().numpy())
+    for T in (796, 1820):
+        for i, what in enumerate(("logp", "lse", "dH")):   # compared as raw bits
+            assert np.array_equal(seen[T][i].view(np.int32 if i < 2 else np.int16),
+                                  seen[Tmax][i][:T].view(np.int32 if i < 2 else np.int16)), (T, what)
+    rows = workloads.sample_rows(796, 16, seed=23)
+    ref_logp, _ = oracle_mod.forward(hb[:796], bits, yb[:796], w.V_true, rows=rows)
+    assert_logp_close(seen[796][0][rows], ref_logp)
+    ref_dH = oracle_mod.backward_dh(hb[:796], bits, yb[:796], g[:796].astype(np.float64), w.V_true,
+                                    rows=rows[:8])
+    dH_bits = seen[796][2][rows[:8]].view(np.uint16).astype(np.uint32) << 16   # bf16 -> fp32 bits
+    assert_grad_close(dH_bits.view(np.float32).astype(np.float64), ref_dH, what="dH rows")
