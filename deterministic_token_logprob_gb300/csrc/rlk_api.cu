@@ -758,6 +758,25 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
   const int32_t n_pm = static_cast<int32_t>(ceil_div(T, PAIR_M));
   int32_t* sched = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + bwd_dz_bytes(T, V_local) +
                                               bwd_run_bytes(T, H, V_local));  // dz, dH, dW
+  // The work-item counters of this call's tile kernels are zeroed first, each stage's own only
+  // (the dH and dW stages may run at once on two streams), so that the kernels follow one
+  // another directly: dH and dW start as programmatic dependents of the kernel before them.
+  {
+    const bool run[3] = {(stages & RLK_BWD_DZ) != 0 && !p_saved && !z_saved,
+                         (stages & RLK_BWD_DH) != 0 && dH != nullptr,
+                         (stages & RLK_BWD_DW) != 0 && dW != nullptr};
+    for (int i = 0; i < 3;) {
+      if (!run[i]) {
+        ++i;
+        continue;
+      }
+      int j = i;
+      while (j < 3 && run[j]) ++j;
+      if (cudaMemsetAsync(sched + i, 0, (j - i) * sizeof(int32_t), s) != cudaSuccess) return RLK_ERR_CUDA;
+      i = j;
+    }
+  }
+  bool after_kernel = false;  // the last operation this call enqueued is a kernel
 
   // 1. dz (bf16) workspace: from saved probabilities, saved logits, or recomputed z tiles
   if (!(stages & RLK_BWD_DZ)) {
@@ -771,12 +790,14 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
         static_cast<int>(vocab_start), static_cast<int>(V_true), dz, Vd, err_flag, T * Vd,
         T * (Vd / 64), T * Vd);
     if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
+    after_kernel = true;
   } else if (z_saved) {
     const int64_t V_valid = std::max<int64_t>(0, std::min<int64_t>(V_true - vocab_start, V_local));
     dz_from_logits_kernel<<<static_cast<unsigned>(T), DZS_THREADS, 0, s>>>(  // one block per row
         z_saved, Vd, y, lse, g, static_cast<int>(Vd), static_cast<int>(V_valid),
         static_cast<int>(vocab_start), static_cast<int>(V_true), dz, Vd, err_flag, T * Vd, T * Vd);
     if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
+    after_kernel = true;
   } else {
     const int eb = f8 ? 1 : 2;  // element bytes of the logit operands
     TileMaps maps{};
@@ -805,7 +826,9 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
     a.out_tma = 1;
     a.err_flag = err_flag;
     a.sched = sched;
+    a.sched_zeroed = 1;
     if ((f8 ? launch_gemm_dz8(maps, a, s) : launch_gemm_dz(maps, a, s)) != cudaSuccess) return RLK_ERR_CUDA;
+    after_kernel = true;
   }
 
   // 2. dH = dz W over this shard's valid columns
@@ -814,6 +837,7 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
     const size_t elem = dH_fp32_partial ? 4 : 2;
     if (V_valid == 0) {
       if (cudaMemsetAsync(dH, 0, static_cast<size_t>(T) * H * elem, s) != cudaSuccess) return RLK_ERR_CUDA;
+      after_kernel = false;
     } else {
       TileMaps maps{};
       GemmArgs a;
@@ -843,7 +867,10 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
       }
       a.err_flag = err_flag;
       a.sched = sched + 1;
+      a.sched_zeroed = 1;
+      a.chained = after_kernel ? 1 : 0;
       if (launch_gemm_dh(maps, a, s) != cudaSuccess) return RLK_ERR_CUDA;
+      after_kernel = true;
     }
   }
 
@@ -873,6 +900,8 @@ rlk_status bwd_impl(const void* h, const void* W, const int64_t* y, const float*
     }
     a.err_flag = err_flag;
     a.sched = sched + 2;
+    a.sched_zeroed = 1;
+    a.chained = after_kernel ? 1 : 0;
     if (launch_gemm_dw(maps, a, s) != cudaSuccess) return RLK_ERR_CUDA;
   }
   return RLK_OK;

@@ -870,9 +870,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   cluster_sync();  // both CTAs' barriers exist before any cross-CTA arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // The kernel that follows in the stream (the forward's leaf-tree merge) may be scheduled
-  // now; it waits for this grid's completion before it reads anything.
+  // The kernel that follows in the stream (the forward's leaf-tree merge, the backward's next
+  // product) may be scheduled now; it waits for this grid's completion before it reads
+  // anything.
   griddep_launch_dependents();
+  // Launched as such a dependent (GemmArgs::chained), this grid has only done its setup so far
+  // (barriers, tensor memory, descriptor prefetch): wait here until the kernel before it has
+  // completed and its writes are visible. Otherwise this returns at once.
+  griddep_wait();
 
   if (warp == 0) {
     if (lane == 0) producer_loop<MODE>(maps, a, smem, full, empty, ring, c);
@@ -899,17 +904,19 @@ template <int MODE>
 cudaError_t launch_gemm(const TileMaps& maps, const GemmArgs& a,
                         cudaStream_t stream) {
   auto kernel = gemm_kernel<MODE>;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = PAIR;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;  // the occupancy query takes the cluster shape only
   // Shared-memory opt-in and resident pairs of this kernel, once per device (both
   // are properties of the device; racing first calls compute the same values).
   static std::atomic<int> resident[64] = {};
@@ -929,8 +936,11 @@ cudaError_t launch_gemm(const TileMaps& maps, const GemmArgs& a,
   clusters = min(clusters, a.n_items);
   cfg.gridDim = dim3(PAIR * clusters, 1, 1);
   if (!a.sched) return cudaErrorInvalidValue;
-  e = cudaMemsetAsync(a.sched, 0, sizeof(int32_t), stream);  // the work-item counter
-  if (e != cudaSuccess) return e;
+  if (!a.sched_zeroed) {
+    e = cudaMemsetAsync(a.sched, 0, sizeof(int32_t), stream);  // the work-item counter
+    if (e != cudaSuccess) return e;
+  }
+  cfg.numAttrs = a.chained ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, kernel, maps, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

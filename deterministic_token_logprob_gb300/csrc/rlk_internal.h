@@ -111,6 +111,9 @@ struct GemmArgs {
   int32_t n_items = 0;
   int32_t n_kb = 0;  // k-blocks of BK per tile
   int32_t* sched = nullptr;  // work-item counter in global memory; the launcher zeroes it
+  int32_t sched_zeroed = 0;  // ... unless the caller zeroed it on the stream already
+  int32_t chained = 0;       // launch as a programmatic dependent of the previous kernel on the
+                             // stream: its setup overlaps that kernel's tail, then it waits for it
   int32_t* err_flag = nullptr;
   // forward / dz
   int32_t V_local = 0, vocab_start = 0, V_true = 0;
