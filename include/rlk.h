@@ -205,10 +205,11 @@ RLK_API rlk_status rlk_linear_logp_bwd(const void* h, const void* W, const int64
  *   RLK_BWD_DZ  recompute the logits and write dz into the workspace
  *   RLK_BWD_DH  dH = dz W from the dz the workspace holds (dH must not be NULL)
  *   RLK_BWD_DW  dW = dz^T h from the dz the workspace holds (dW must not be NULL)
- * and every other argument is as in rlk_linear_logp_bwd. A stage launches exactly
- * the kernel, with exactly the arguments, that rlk_linear_logp_bwd launches for it,
- * so stages run one call at a time in the order DZ, DH, DW with one workspace give
- * the bits of a single rlk_linear_logp_bwd call. The workspace must stay untouched
+ * and every other argument is as in rlk_linear_logp_bwd. A stage launches the kernel
+ * that rlk_linear_logp_bwd launches for it, on the same operands in the same work order
+ * (only how it follows the launch before it differs), so stages run one call at a time
+ * in the order DZ, DH, DW with one workspace give the bits of a single
+ * rlk_linear_logp_bwd call. The workspace must stay untouched
  * from the DZ call until the last call that reads its dz. Each stage has its own
  * work-item counter in the workspace and only RLK_BWD_DH uses its fp32 running sum,
  * so once the DZ stage has completed, the DH and DW stages may run on two streams
@@ -415,8 +416,10 @@ RLK_API rlk_status rlk_selftest_wait_timeout(const void* h, const void* W, const
  * stores, the dz passes, the leaf-tree reads) they check the index against the extent of
  * the buffer, and before every tensor copy they check the rules of its coordinates (the
  * innermost one a multiple of 16 bytes, a store's never negative). A failed check ORs
- * RLK_FLAG_BOUNDS into *err_flag and skips the access instead of trapping, so the context
- * stays usable. Results of a build with checks are bit-identical to the plain build's.
+ * RLK_FLAG_BOUNDS into *err_flag instead of trapping and skips the access (a load's
+ * misaligned coordinate is rounded down instead, so the pipeline's byte counts still
+ * complete), so the context stays usable. Results of a build with checks are bit-identical
+ * to the plain build's.
  *
  * rlk_debug_checks: 1 for a library built with the checks, else 0.
  * rlk_selftest_bounds_check: the unsharded forward (arguments as rlk_linear_logp_fwd) told
