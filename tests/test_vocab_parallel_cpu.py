@@ -1,5 +1,5 @@
 """The cross-rank exchange of vocab-parallel linear_logp (deterministic_token_logprob_gb300.
-vocab_parallel) on CPU: 2 and 4 gloo ranks.
+vocab_parallel) on CPU: 2, 4 and 8 gloo ranks.
 
 The exchange must hand the merge and the dH sum exactly the inputs the single-process
 emulation gives them (the shards' statistics stacked in vocab order; the dH partials summed
@@ -85,7 +85,7 @@ def _worker(rank, world, port, out):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world", [2, 4])
+@pytest.mark.parametrize("world", [2, 4, 8])
 def test_vocab_parallel_exchange_matches_single_process(world):
     port = _free_port()
     with mp.Manager() as m:
