@@ -108,6 +108,18 @@ def traffic_per_launch(stage: str):
     return k["traffic_bytes_per_launch"], f"ncu capture: {rec.get('command')}"
 
 
+def print_line(line: dict):
+    """Print the JSON line as the last thing on stdout: C-level stdio output buffered by
+    libraries (a communication library's version banner, say) is flushed first."""
+    try:
+        import ctypes
+        ctypes.CDLL(None).fflush(None)
+    except (OSError, AttributeError):
+        pass
+    sys.stdout.flush()
+    print(json.dumps(line), flush=True)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -502,7 +514,7 @@ def run_gpu(args, w: workloads.Workload, rank: int, world: int, local_rank: int)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        print_line(line)
 
 
 STAGE_LABEL = {"fwd": "forward tile GEMM + online statistics (call incl. leaf tree)",
@@ -1014,6 +1026,74 @@ def e2e(rlk, torch, path, w, d, device, args, gpu_id=None, world=1):
     return out
 
 
+def run_vocab_parallel(args, w: workloads.Workload, rank: int, world: int, local_rank: int):
+    """--parallel vocab: the ranks hold one contiguous shard of W each (shard_bounds(V, V_true, S),
+    S = the number of ranks) and the same batch; a step is the forward and backward across the
+    group (deterministic_token_logprob_gb300.vocab_parallel: all-gather of the shard statistics
+    and rlk_lse_merge; fp32 dH partials summed in rank order by all-to-all, rlk_shard_sum_bf16
+    and all-gather; dW rows local). The total work is fixed, so this is strong scaling."""
+    import torch
+
+    import deterministic_token_logprob_gb300 as rlk
+    from deterministic_token_logprob_gb300 import build as libbuild
+    from deterministic_token_logprob_gb300 import vocab_parallel as vp
+    if rank == 0:
+        libbuild.build()
+    torch.distributed.barrier()
+    device = torch.device("cuda", local_rank)
+    peaks, peaks_src = load_peaks()
+    start, n = vp.shard_of_rank(w.V, w.V_true)
+    d = workloads.make_inputs(w, with_W=False)   # the same batch on every rank (seed 0)
+    W_bits = workloads.make_W(w.V, w.H, seed=0)[start:start + n]
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)  # noqa: E731
+    h, W = bf(d["h"]), bf(W_bits)
+    y, g = torch.from_numpy(d["y"]).to(device), torch.from_numpy(d["g"]).to(device)
+    fws = torch.empty(rlk.fwd_workspace_bytes(w.T, w.H, n), dtype=torch.uint8, device=device)
+    bws = torch.empty(rlk.bwd_workspace_bytes(w.T, w.H, n), dtype=torch.uint8, device=device)
+
+    def step():
+        _, lse = vp.linear_logp_fwd_tp(h, W, y, w.V_true, w.V, workspace=fws)
+        vp.linear_logp_bwd_tp(h, W, y, lse, g, w.V_true, w.V, workspace=bws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    K = args.steps
+    sampler = ClockSampler(gpu_uuid(torch, device)) if rank == 0 else None
+    if sampler:
+        sampler.wait_running()
+    torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    if sampler:
+        sampler.mark_start()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(K):
+        step()
+    b.record()
+    torch.cuda.synchronize(device)
+    if sampler:
+        sampler.mark_end()
+    torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    total_ms = max_over_ranks(a.elapsed_time(b), world, device)
+    ms = total_ms / K
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    step_flops = 3.0 * 2.0 * w.T * w.H * w.V_true
+    line = {"metric": METRIC, "value": w.T / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "strong", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(config_dict(w, world), parallelism=f"vocab{world}",
+                           global_tokens=w.T, shard_of_rank_0=list(rlk.shard_bounds(w.V, w.V_true, world)[0])),
+            "gpu_launches": K * 7,  # per rank and step: forward 2 + merge 1, backward 3 + sum 1
+            "step_roofline": {"flops_counted": step_flops,
+                              "frac_of_burst": step_flops / (peak * world * 1e12) / (ms / 1e3),
+                              "peak_source": f"{peaks_src} bf16 burst x {world} GPUs"},
+            "clocks": clocks}
+    if rank == 0:
+        print_line(line)
+
+
 def run_case(args):
     """One stage of the path at the Qwen3-8B H and V with --tokens tokens, timed per call
     with CUDA events (for per-kernel timing and small-case ncu captures)."""
@@ -1079,6 +1159,9 @@ def main():
     ap.add_argument("--impl", choices=["rlk", "reference"], default="rlk")
     ap.add_argument("--workload", choices=["qwen3_8b", "qwen3_30b_tp2", "tiny"], default="qwen3_8b")
     ap.add_argument("--quick", action="store_true", help="skip the forward-only, e2e and CPU legs")
+    ap.add_argument("--parallel", choices=["replicas", "vocab"], default="replicas",
+                    help="replicas: one independent batch per rank (default); vocab: one batch, "
+                         "W split into one vocab shard per rank (1, 2, 4 or 8 ranks)")
     ap.add_argument("--case", choices=["fwd", "dz", "dh", "dw", "fwd8", "dz8"], default=None,
                     help="time one stage only (dz alone; dh / dw each after its dz)")
     ap.add_argument("--tokens", type=int, default=1024, help="tokens for --case")
@@ -1105,16 +1188,33 @@ def main():
     if args.impl == "reference":
         run_reference(args, w, rank, world)
         return
-    if world > 1:
+    vocab = args.parallel == "vocab"
+    if vocab and world not in (1, 2, 4, 8):
+        ap.error("--parallel vocab needs 1, 2, 4 or 8 ranks")
+    if world > 1 or vocab:
         import torch
         torch.cuda.set_device(local_rank)
-        torch.distributed.init_process_group("nccl")
-    try:
-        run_gpu(args, w, rank, world, local_rank)
-    finally:
         if world > 1:
+            torch.distributed.init_process_group("nccl")
+        else:   # a one-rank group, so that the exchange runs its collectives
+            torch.distributed.init_process_group(
+                "nccl", init_method=f"tcp://127.0.0.1:{_free_port()}", rank=0, world_size=1)
+    try:
+        if vocab:
+            run_vocab_parallel(args, w, rank, world, local_rank)
+        else:
+            run_gpu(args, w, rank, world, local_rank)
+    finally:
+        if world > 1 or vocab:
             import torch
             torch.distributed.destroy_process_group()
+
+
+def _free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
 
 
 if __name__ == "__main__":
