@@ -90,8 +90,14 @@ def linear_logp_fwd_tp(h: torch.Tensor, W_local: torch.Tensor, y: torch.Tensor, 
     start, n = shard_of_rank(V, V_true, group)
     if W_local.shape[0] != n:
         raise ValueError(f"rank's W shard has {W_local.shape[0]} rows, its shard has {n}")
-    part = rlk.linear_logp_fwd(h, W_local, y, V_true, vocab_start=start, partial=True,
-                               err_flag=err_flag, workspace=workspace)
+    if n == 0:
+        # a small vocabulary can leave a rank no rows: its statistics are the merge's identity
+        # (m = -inf, s = 0, zt = -inf), which the merge passes over bit for bit
+        part = torch.tensor([float("-inf"), 0.0, float("-inf")], dtype=torch.float32,
+                            device=h.device).repeat(h.shape[0], 1)
+    else:
+        part = rlk.linear_logp_fwd(h, W_local, y, V_true, vocab_start=start, partial=True,
+                                   err_flag=err_flag, workspace=workspace)
     return rlk.lse_merge(gather_stats(part, group))
 
 
@@ -104,7 +110,12 @@ def linear_logp_bwd_tp(h: torch.Tensor, W_local: torch.Tensor, y: torch.Tensor, 
     start, n = shard_of_rank(V, V_true, group)
     if W_local.shape[0] != n:
         raise ValueError(f"rank's W shard has {W_local.shape[0]} rows, its shard has {n}")
-    dHp, dW = rlk.linear_logp_bwd(h, W_local, y, lse, g, V_true, vocab_start=start,
-                                  dH_fp32_partial=True, want_dW=want_dW, err_flag=err_flag,
-                                  workspace=workspace)
+    if n == 0:  # no rows on this rank: a zero dH partial, no dW rows
+        T, H = h.shape
+        dHp = torch.zeros((T, H), dtype=torch.float32, device=h.device)
+        dW = torch.empty((0, H), dtype=torch.float32, device=h.device) if want_dW else None
+    else:
+        dHp, dW = rlk.linear_logp_bwd(h, W_local, y, lse, g, V_true, vocab_start=start,
+                                      dH_fp32_partial=True, want_dW=want_dW, err_flag=err_flag,
+                                      workspace=workspace)
     return sum_dH_partials(dHp, group), dW

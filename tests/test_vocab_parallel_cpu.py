@@ -110,3 +110,75 @@ def test_shard_of_rank_requires_a_supported_group_size():
         rlk.shard_bounds(151936, 151669, 3)
     # two ranks split at the super-shard boundary, as the emulated Qwen3-30B workload does
     assert rlk.shard_bounds(151936, 151669, 2) == list(workloads.QWEN3_30B_TP2.shards)
+
+
+def _worker_small_vocab(rank, world, port, out):
+    # linear_logp_fwd_tp / linear_logp_bwd_tp end to end on CPU ranks, with the library's calls
+    # replaced by stand-ins (the oracle's shard statistics and merge, seeded fp32 dH partials),
+    # for a vocabulary so small that some ranks hold no rows
+    import torch.distributed as dist
+
+    import oracle
+    from deterministic_token_logprob_gb300 import _binding
+    from deterministic_token_logprob_gb300 import vocab_parallel as vp
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        oracle.build()
+        T, H, V, Vt = 9, 32, 3000, 2900
+        d = workloads.make_inputs(workloads.Workload("vps", T=T, H=H, V=V, V_true=Vt, seed=8))
+        calls = []
+
+        def bits(t):
+            return t.view(torch.int16).numpy().view(np.uint16)
+
+        def fake_fwd(h, W, y, V_true, vocab_start=0, partial=False, **kw):
+            calls.append("fwd")
+            m, s, zt = oracle.shard_stats(bits(h), bits(W), y.numpy(), vocab_start, V_true)
+            return torch.from_numpy(np.stack([m, s, zt], axis=1).astype(np.float32))
+
+        def fake_merge(parts, **kw):
+            p = parts.double().numpy()
+            logp, lse = oracle.lse_merge(p[:, :, 0], p[:, :, 1], p[:, :, 2])
+            return torch.from_numpy(logp.astype(np.float32)), torch.from_numpy(lse.astype(np.float32))
+
+        def fake_bwd(h, W, y, lse, g, V_true, vocab_start=0, want_dW=True, **kw):
+            calls.append("bwd")
+            return _partial(rank, h.shape[0], h.shape[1]), torch.zeros((W.shape[0], h.shape[1]))
+
+        _binding.linear_logp_fwd = fake_fwd
+        _binding.lse_merge = fake_merge
+        _binding.linear_logp_bwd = fake_bwd
+        _binding.shard_sum_bf16 = _host_sum_bf16
+        start, n = vp.shard_of_rank(V, Vt)
+        h = torch.from_numpy(d["h"].view(np.int16)).view(torch.bfloat16)
+        W = torch.from_numpy(d["W"][start:start + n].view(np.int16)).view(torch.bfloat16)
+        y, g = torch.from_numpy(d["y"]), torch.from_numpy(d["g"])
+        logp, lse = vp.linear_logp_fwd_tp(h, W, y, Vt, V)
+        dH, dW = vp.linear_logp_bwd_tp(h, W, y, lse, g, Vt, V)
+        ref_logp, _ = oracle.forward(d["h"], d["W"], d["y"], Vt)
+        sizes = [k for _, k in _binding.shard_bounds(V, Vt, world)]
+        parts = [(_partial(r, T, H) if sizes[r] else torch.zeros((T, H))) for r in range(world)]
+        ref_dH = _host_sum_bf16(torch.stack(parts))
+        out[rank] = (n, calls, float(np.max(np.abs(logp.double().numpy() - ref_logp))),
+                     torch.equal(dH.view(torch.int16), ref_dH.view(torch.int16)), tuple(dW.shape))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_ranks_without_vocabulary_rows_take_part_in_the_exchange():
+    world = 4
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_worker_small_vocab, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    sizes = [res[r][0] for r in range(world)]
+    assert sizes[0] > 0 and 0 in sizes, sizes      # this vocabulary leaves some ranks empty
+    for r in range(world):
+        n, calls, err, dH_ok, dW_shape = res[r]
+        assert calls == ([] if n == 0 else ["fwd", "bwd"]), (r, calls)   # empty: no library call
+        assert err < 1e-5, (r, err)
+        assert dH_ok, r
+        assert dW_shape == (n, 32)
