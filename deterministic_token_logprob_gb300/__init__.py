@@ -15,3 +15,4 @@ from ._binding import (  # noqa: F401
     linear_logp_fwd_save_probs, lse_merge, quantize_rows_e4m3, saved_logits_buffer,
     saved_logits_bytes, saved_probs_bytes, selftest_bounds_check, selftest_wait_timeout,
     shard_bounds, shard_sum_bf16, version)
+from .autograd import LinearLogp, linear_logp  # noqa: F401
