@@ -629,12 +629,27 @@ def tp2_rank_calls_leg(rlk, torch, device, args, peak):
         K = max(args.steps, 10)
         f_ms, fb_ms = _time_calls(torch, device, fwd, K), _time_calls(torch, device, fwd_bwd, K)
         flops = 2.0 * T * H * min(n0, Vt - a0)
-        out[str(T)] = {"fwd_ms": f_ms, "fwd_bwd_ms": fb_ms,
+        # memory of one forward + backward call pair whose every buffer (workspaces, statistics,
+        # dH partial, dW rows) the binding allocates, with the inputs already resident
+        torch.cuda.synchronize(device)
+        torch.cuda.empty_cache()
+        torch.cuda.reset_peak_memory_stats(device)
+        m_alloc, m_res = torch.cuda.memory_allocated(device), torch.cuda.memory_reserved(device)
+        p0 = rlk.linear_logp_fwd(h, W, y, Vt, vocab_start=a0, partial=True)
+        lp, ls = rlk.lse_merge(torch.stack([p0, parts[1]]))
+        dh_m, dw_m = rlk.linear_logp_bwd(h, W, y, ls, g, Vt, vocab_start=a0, dH_fp32_partial=True)
+        torch.cuda.synchronize(device)
+        mem = {"peak_allocated_delta_MB": (torch.cuda.max_memory_allocated(device) - m_alloc) / 2**20,
+               "peak_reserved_delta_MB": (torch.cuda.max_memory_reserved(device) - m_res) / 2**20}
+        del p0, lp, ls, dh_m, dw_m
+        out[str(T)] = {"fwd_ms": f_ms, "fwd_bwd_ms": fb_ms, "memory": mem,
                        "fwd_tflops": flops / (f_ms / 1e3) / 1e12,
                        "fwd_bwd_tflops": 3 * flops / (fb_ms / 1e3) / 1e12,
                        "fwd_frac_of_burst": flops / (f_ms / 1e3) / 1e12 / peak}
     out["note"] = ("per-rank single-operator times; the backward's recompute GEMM is not "
-                   "counted in fwd_bwd_tflops (3 GEMM-equivalents credited, 4 run)")
+                   "counted in fwd_bwd_tflops (3 GEMM-equivalents credited, 4 run); memory = peak "
+                   "delta of one fwd + bwd call pair with every buffer allocated by the binding "
+                   "(dz workspace, fp32 dH partial, fp32 dW rows of the shard), inputs excluded")
     return out
 
 
